@@ -1,0 +1,173 @@
+"""fp64 CPU oracle for scaled dot-product attention -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline legs of
+``bench.py`` may import this package.  The CUDA library never loads it, and it
+never loads the CUDA library.
+
+The arithmetic lives in ``sdpa_oracle.c`` (plain C, fp64, one query row at a
+time, OpenMP over rows); this module only compiles it with gcc and marshals
+arrays.  It computes the five steps printed in "Profiling attention in PyTorch:
+kernels, backends and where the time goes" (news.bpdata.com), section "Naiv
+causal attention", and in "PyTorch attention profiling: Flash, cuDNN and Math
+backends compared" (dev.smart-guide.co.kr), section 1: matmul(q, k^T), times
+scale, masked_fill(mask, -inf), softmax over keys, matmul(attn, v) -- with the
+math backend's safe softmax (a fully removed row gives zeros) from the
+math-backend sections of the same pages.
+
+Parity pins (see ``tests/test_oracle.py``): exact-decimal brute force on tiny
+shapes, closed forms (causal row 0 -> v[0]; q = 0 -> prefix mean; one allowed
+key -> that value row; equal keys -> mean of allowed values), invariants
+(weights sum to one, linearity in v, key/value permutation and key-shift
+invariance, zero rows for fully removed queries) and torch's CPU math backend
+in fp64.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "sdpa_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle_sdpa.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def compile_source(src: str, lib_path: str) -> str:
+    """gcc -O2, OpenMP, no fast-math (fp64 rounding follows the source order)."""
+    tmp = lib_path + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared", "-o", tmp, src, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, lib_path)
+    return lib_path
+
+
+def build(force: bool = False) -> str:
+    """Compile ``sdpa_oracle.c`` into ``liboracle_sdpa.so`` beside it."""
+    if (not force and os.path.exists(_LIB)
+            and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
+        return _LIB
+    return compile_source(_SRC, _LIB)
+
+
+def load_variant(lib_path: str):
+    """Bind another build of the oracle source (the tests use this to show
+    that deliberately broken copies fail the pins)."""
+    return _bind(ctypes.CDLL(lib_path))
+
+
+def _bind(lib):
+    d, i64, u8p = ctypes.POINTER(ctypes.c_double), ctypes.c_int64, ctypes.c_void_p
+    lib.oracle_sdpa_fp64.argtypes = [d, d, d, d, i64, i64, i64, i64, u8p,
+                                     ctypes.c_int, ctypes.c_double]
+    lib.oracle_sdpa_fp64.restype = ctypes.c_int
+    lib.oracle_sdpa_rows_fp64.argtypes = [d, d, d, i64, i64, i64, i64, u8p,
+                                          ctypes.c_int, ctypes.c_double,
+                                          ctypes.POINTER(ctypes.c_int64), i64, d]
+    lib.oracle_sdpa_rows_fp64.restype = ctypes.c_int
+    lib.oracle_num_threads.argtypes = []
+    lib.oracle_num_threads.restype = ctypes.c_int
+    return lib
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            _lib = _bind(ctypes.CDLL(build()))
+    return _lib
+
+
+def num_threads() -> int:
+    """OpenMP threads the oracle runs on (``OMP_NUM_THREADS`` caps it)."""
+    return int(_load().oracle_num_threads())
+
+
+def _as_f64(x) -> np.ndarray:
+    """Widen a torch tensor or array exactly to a dense float64 numpy array."""
+    try:
+        import torch
+        if isinstance(x, torch.Tensor):
+            x = x.detach().to("cpu", torch.float64).contiguous().numpy()
+    except ImportError:  # pragma: no cover - torch is always present here
+        pass
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+def _as_mask(mask, L):
+    if mask is None:
+        return None
+    try:
+        import torch
+        if isinstance(mask, torch.Tensor):
+            mask = mask.detach().cpu().numpy()
+    except ImportError:  # pragma: no cover
+        pass
+    m = np.ascontiguousarray(np.asarray(mask) != 0, dtype=np.uint8)
+    if m.shape != (L, L):
+        raise ValueError(f"mask must be [L, L] = [{L}, {L}], got {m.shape}")
+    return m
+
+
+def _shape4(q):
+    if q.ndim == 3:
+        return (1,) + q.shape
+    if q.ndim == 4:
+        return q.shape
+    raise ValueError(f"q must be rank 3 [H, L, D] or rank 4 [B, H, L, D], got {q.shape}")
+
+
+def default_scale(D: int) -> float:
+    """1/sqrt(head_dim): the scale the NaiveCausalAttention module sets in its
+    constructor on both profiling pages."""
+    return 1.0 / math.sqrt(D)
+
+
+def sdpa(q, k, v, mask=None, is_causal=False, scale=None, _lib_override=None) -> np.ndarray:
+    """Full attention output in fp64, same rank as ``q`` ([H,L,D] or [B,H,L,D]).
+
+    ``mask``: optional [L, L], nonzero = removed (masked_fill polarity).
+    ``scale``: None -> 1/sqrt(D)."""
+    q, k, v = _as_f64(q), _as_f64(k), _as_f64(v)
+    if not (q.shape == k.shape == v.shape):
+        raise ValueError("q, k, v must share one shape")
+    B, H, L, D = _shape4(q)
+    m = _as_mask(mask, L)
+    s = default_scale(D) if scale is None else float(scale)
+    out = np.empty_like(q)
+    dp = ctypes.POINTER(ctypes.c_double)
+    lib = _lib_override if _lib_override is not None else _load()
+    rc = lib.oracle_sdpa_fp64(
+        q.ctypes.data_as(dp), k.ctypes.data_as(dp), v.ctypes.data_as(dp),
+        out.ctypes.data_as(dp), B, H, L, D,
+        None if m is None else m.ctypes.data, int(bool(is_causal)), s)
+    if rc != 0:
+        raise RuntimeError("oracle_sdpa_fp64 failed")
+    return out
+
+
+def sdpa_rows(q, k, v, rows, mask=None, is_causal=False, scale=None,
+              _lib_override=None) -> np.ndarray:
+    """Output rows for the (b, h, i) triples in ``rows`` (shape [n, 3]); for
+    rank-3 inputs pass b = 0.  Returns [n, D] fp64."""
+    q, k, v = _as_f64(q), _as_f64(k), _as_f64(v)
+    B, H, L, D = _shape4(q)
+    m = _as_mask(mask, L)
+    idx = np.ascontiguousarray(np.asarray(rows, dtype=np.int64).reshape(-1, 3))
+    s = default_scale(D) if scale is None else float(scale)
+    out = np.empty((idx.shape[0], D), dtype=np.float64)
+    dp = ctypes.POINTER(ctypes.c_double)
+    lib = _lib_override if _lib_override is not None else _load()
+    rc = lib.oracle_sdpa_rows_fp64(
+        q.ctypes.data_as(dp), k.ctypes.data_as(dp), v.ctypes.data_as(dp),
+        B, H, L, D, None if m is None else m.ctypes.data, int(bool(is_causal)), s,
+        idx.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), idx.shape[0],
+        out.ctypes.data_as(dp))
+    if rc != 0:
+        raise RuntimeError("oracle_sdpa_rows_fp64 failed (row index out of range?)")
+    return out
