@@ -1,0 +1,138 @@
+/*
+ * sdpa.h -- C ABI of the GB300 (sm_103a) fused scaled dot-product attention
+ * forward.
+ *
+ * OPERATION.  For every (batch b, head h) and query row i:
+ *
+ *     out[b,h,i,:] = sum_j softmax_j( scale * q[b,h,i,:] . k[b,h,j,:]
+ *                                     with removed keys at -inf ) * v[b,h,j,:]
+ *
+ * i.e. the five steps matmul(q, k^T), times scale, masked_fill(mask, -inf),
+ * softmax over keys, matmul(attn, v) of the NaiveCausalAttention module in
+ * "Profiling attention in PyTorch: kernels, backends and where the time goes"
+ * (news.bpdata.com), section "Naiv causal attention", and of section 1 of
+ * "PyTorch attention profiling: Flash, cuDNN and Math backends compared"
+ * (dev.smart-guide.co.kr).  The user-facing call there is
+ * F.scaled_dot_product_attention(q, k, v, is_causal=True) (same pages, SDPA
+ * sections); this ABI takes the same arguments as raw device pointers.
+ *
+ *   - causal (is_causal != 0): query i sees keys j <= i.
+ *   - explicit mask: mask[i*L + j] != 0 removes key j for query i, the
+ *     masked_fill polarity (1 = masked out).  One [L, L] mask serves every
+ *     (b, h).
+ *   - a query with no admissible key yields a zero row (the math backend's
+ *     "safe softmax", same pages, math-backend sections), never NaN.
+ *   - rank-3 inputs [H, L, D] are treated as rank-4 [1, H, L, D] and reach the
+ *     same fused kernel ("PyTorch 2.14 SDPA: rank-3 inputs now take the fused
+ *     kernels", daker.dacon.io, sections on the rank-3 problem and on what
+ *     changed in 2.14); results are bit-identical to the rank-4 call.
+ *
+ * Computation: one GPU kernel launch per call; 16-bit inputs on tensor cores
+ * with fp32 accumulation, the softmax in fp32, probabilities rounded to the
+ * input type before the second product, output rounded to nearest even.
+ */
+#ifndef SDPA_GB300_H
+#define SDPA_GB300_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define SDPA_API __attribute__((visibility("default")))
+#else
+#define SDPA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum sdpa_status {
+  SDPA_OK = 0,
+  SDPA_ERR_NULL = 1,            /* a required pointer argument is NULL */
+  SDPA_ERR_RANK = 2,            /* rank is not 3 or 4 */
+  SDPA_ERR_SHAPE = 3,           /* D not 64 or 128, or a dimension < 1, or too large */
+  SDPA_ERR_DTYPE = 4,           /* dtype is not SDPA_BF16 / SDPA_FP16 */
+  SDPA_ERR_LAYOUT = 5,          /* inner stride != 1, other strides not multiples of 8
+                                   elements (16 bytes), zero stride on a dimension > 1,
+                                   or a pointer not 16-byte aligned */
+  SDPA_ERR_ARG = 6,             /* causal and mask both given, or out overlaps q/k/v/mask,
+                                   or a NaN/inf scale other than the NaN default */
+  SDPA_ERR_CUDA = 7,            /* the CUDA runtime/driver reported an error (launch,
+                                   tensor-map encoding, no device) */
+  SDPA_ERR_DEVICE_TIMEOUT = 8,  /* a kernel barrier wait ran out of time (see
+                                   sdpa_last_device_status) */
+  SDPA_ERR_DEVICE = 9           /* the current device is not an sm_103 GPU */
+} sdpa_status;
+
+typedef enum sdpa_dtype {
+  SDPA_BF16 = 0,
+  SDPA_FP16 = 1
+} sdpa_dtype;
+
+/*
+ * sdpa_forward -- launch the fused attention forward on `stream`.
+ *
+ * q, k, v, out : DEVICE pointers to 16-bit elements of type `dtype`; all four
+ *                share one logical shape.  The caller owns them; the call
+ *                neither frees nor retains them.
+ * rank         : 3 for [H, L, D], 4 for [B, H, L, D].
+ * shape        : `rank` extents (host array).  D must be 64 or 128; L >= 1
+ *                (any value, including ragged ones not divisible by 128).
+ * *_stride     : `rank` strides in ELEMENTS (host arrays), so any strided view
+ *                (for example a [B, L, H, D] buffer viewed as [B, H, L, D])
+ *                is consumed in place with no transpose.  The innermost (D)
+ *                stride must be 1; every other stride must be a multiple of
+ *                8 elements and non-zero unless its extent is 1.
+ * is_causal    : nonzero for the causal triangle.
+ * mask         : NULL, or a DEVICE pointer to a dense row-major [L, L] byte
+ *                matrix (nonzero = removed).  Not allowed together with
+ *                is_causal.
+ * scale        : multiplier of q.k; NaN selects the default 1/sqrt(D) (the
+ *                module's scale on both profiling pages).
+ * stream       : a cudaStream_t (NULL = legacy default stream).
+ *
+ * Returns SDPA_OK once the kernel is enqueued (asynchronous: results are
+ * ready when the stream reaches it), or an error code.  Argument errors are
+ * detected on the host before any CUDA call and launch nothing.  No device
+ * memory is allocated per call.  Thread-compatible: concurrent calls must use
+ * different streams.
+ */
+SDPA_API sdpa_status sdpa_forward(const void* q, const void* k, const void* v, void* out,
+                         sdpa_dtype dtype, int rank, const int64_t* shape,
+                         const int64_t* q_stride, const int64_t* k_stride,
+                         const int64_t* v_stride, const int64_t* o_stride,
+                         int is_causal, const uint8_t* mask, float scale, void* stream);
+
+/* Human-readable name of a status code (static storage, never NULL). */
+SDPA_API const char* sdpa_status_string(sdpa_status status);
+
+/*
+ * sdpa_last_device_status -- synchronise `stream`, then report whether any
+ * kernel since the previous query gave up on a barrier wait (every wait in
+ * the kernel is bounded in time; on expiry the kernel stops, frees its
+ * resources and sets a device status word instead of hanging).  Returns
+ * SDPA_OK, SDPA_ERR_DEVICE_TIMEOUT (the word is then cleared), or
+ * SDPA_ERR_CUDA.  When `detail` is not NULL it receives the raw status bits.
+ */
+SDPA_API sdpa_status sdpa_last_device_status(void* stream, uint32_t* detail);
+
+/* ABI version: major * 10000 + minor * 100 + patch. */
+SDPA_API int sdpa_version(void);
+
+/*
+ * Test hooks (not for production use).
+ * sdpa_debug_set_wait_limit_ns: bound on a single barrier wait inside the
+ *   kernel (default 1e9 ns); 0 restores the default.
+ * sdpa_debug_withhold_q_load: when nonzero, subsequent launches never load
+ *   the query tile, so every consumer wait runs out: the kernel must return
+ *   with SDPA_ERR_DEVICE_TIMEOUT reported by sdpa_last_device_status and the
+ *   context must stay usable.
+ */
+SDPA_API void sdpa_debug_set_wait_limit_ns(uint64_t ns);
+SDPA_API void sdpa_debug_withhold_q_load(int enable);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SDPA_GB300_H */

@@ -1,0 +1,162 @@
+"""GB300 (sm_103a) fused scaled dot-product attention forward.
+
+A thin ctypes binding over the C ABI declared in ``include/sdpa.h``: the
+Python functions carry the C names and only marshal arguments (pointers,
+shapes, strides, the current stream).  Every step of the computation runs in
+the CUDA kernel of ``libsdpa_gb300.so``; there is no Python or CPU fallback,
+and importing this package fails loudly when the library is missing.
+
+    out = sdpa_forward(q, k, v, is_causal=True)          # torch tensors on cuda
+    out = sdpa_forward(q, k, v, mask=m)                  # m: [L, L], 1 = masked out
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+from . import _build
+
+__all__ = ["sdpa_forward", "sdpa_forward_raw", "sdpa_status_string", "sdpa_last_device_status",
+           "sdpa_version", "SdpaError", "load_library", "LIB_PATH", "STATUS",
+           "sdpa_debug_set_wait_limit_ns", "sdpa_debug_withhold_q_load"]
+
+LIB_PATH = _build.LIB_PATH
+
+STATUS = {
+    0: "SDPA_OK", 1: "SDPA_ERR_NULL", 2: "SDPA_ERR_RANK", 3: "SDPA_ERR_SHAPE",
+    4: "SDPA_ERR_DTYPE", 5: "SDPA_ERR_LAYOUT", 6: "SDPA_ERR_ARG", 7: "SDPA_ERR_CUDA",
+    8: "SDPA_ERR_DEVICE_TIMEOUT", 9: "SDPA_ERR_DEVICE",
+}
+SDPA_BF16, SDPA_FP16 = 0, 1
+
+
+class SdpaError(RuntimeError):
+    def __init__(self, status: int, where: str = "sdpa_forward"):
+        self.status = int(status)
+        super().__init__(f"{where}: {sdpa_status_string(status)} (status {status})")
+
+
+_lib = None
+
+
+def load_library(path: str | None = None):
+    """Load the shared library (once).  Raises if it has not been built."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise ImportError(
+            f"{p} is missing: build it with scaled_dot_product_forward_gb300._build.build() "
+            "(the CUDA path is the only path; there is no fallback)")
+    lib = ctypes.CDLL(p)
+    i64p, vp = ctypes.POINTER(ctypes.c_int64), ctypes.c_void_p
+    lib.sdpa_forward.argtypes = [vp, vp, vp, vp, ctypes.c_int, ctypes.c_int, i64p,
+                                 i64p, i64p, i64p, i64p, ctypes.c_int, vp, ctypes.c_float, vp]
+    lib.sdpa_forward.restype = ctypes.c_int
+    lib.sdpa_status_string.argtypes = [ctypes.c_int]
+    lib.sdpa_status_string.restype = ctypes.c_char_p
+    lib.sdpa_last_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
+    lib.sdpa_last_device_status.restype = ctypes.c_int
+    lib.sdpa_version.argtypes = []
+    lib.sdpa_version.restype = ctypes.c_int
+    lib.sdpa_debug_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+    lib.sdpa_debug_set_wait_limit_ns.restype = None
+    lib.sdpa_debug_withhold_q_load.argtypes = [ctypes.c_int]
+    lib.sdpa_debug_withhold_q_load.restype = None
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def sdpa_status_string(status: int) -> str:
+    return load_library().sdpa_status_string(int(status)).decode()
+
+
+def sdpa_version() -> int:
+    return int(load_library().sdpa_version())
+
+
+def sdpa_debug_set_wait_limit_ns(ns: int) -> None:
+    load_library().sdpa_debug_set_wait_limit_ns(int(ns))
+
+
+def sdpa_debug_withhold_q_load(enable: bool) -> None:
+    load_library().sdpa_debug_withhold_q_load(1 if enable else 0)
+
+
+def _arr(vals):
+    return (ctypes.c_int64 * len(vals))(*[int(x) for x in vals])
+
+
+def sdpa_forward_raw(q_ptr: int, k_ptr: int, v_ptr: int, out_ptr: int, dtype: int, rank: int,
+                     shape, q_stride, k_stride, v_stride, o_stride, is_causal: bool,
+                     mask_ptr: int | None, scale: float, stream: int) -> int:
+    """Call the C ABI with plain integers (device addresses, element strides,
+    a cudaStream_t handle).  Returns the status code without raising."""
+    lib = load_library()
+    return int(lib.sdpa_forward(
+        ctypes.c_void_p(q_ptr), ctypes.c_void_p(k_ptr), ctypes.c_void_p(v_ptr),
+        ctypes.c_void_p(out_ptr), int(dtype), int(rank), _arr(shape),
+        _arr(q_stride), _arr(k_stride), _arr(v_stride), _arr(o_stride),
+        1 if is_causal else 0, ctypes.c_void_p(mask_ptr) if mask_ptr else None,
+        ctypes.c_float(scale), ctypes.c_void_p(stream) if stream else None))
+
+
+def sdpa_forward(q, k, v, out=None, *, is_causal: bool = False, mask=None, scale=None,
+                 stream=None):
+    """Fused attention forward on torch CUDA tensors.
+
+    q, k, v: [H, L, D] or [B, H, L, D], bf16 or fp16, any strides with the
+    last one 1.  mask: optional [L, L] bool/uint8 on the same device (True /
+    nonzero = removed).  scale: None -> 1/sqrt(D).  out: optional
+    preallocated output (may be a strided view).  Launches on ``stream`` (a
+    torch.cuda.Stream) or the current stream; returns ``out``.
+    """
+    import torch
+
+    if q.dtype == torch.bfloat16:
+        dt = SDPA_BF16
+    elif q.dtype == torch.float16:
+        dt = SDPA_FP16
+    else:
+        raise SdpaError(4)
+    if k.dtype != q.dtype or v.dtype != q.dtype:
+        raise SdpaError(4)
+    if q.shape != k.shape or q.shape != v.shape:
+        raise SdpaError(3)
+    if out is None:
+        out = torch.empty_like(q, memory_format=torch.contiguous_format)
+    elif out.dtype != q.dtype or out.shape != q.shape:
+        raise SdpaError(3)
+    mptr = None
+    if mask is not None:
+        if mask.dtype == torch.bool:
+            mask = mask.view(torch.uint8)
+        if mask.dtype != torch.uint8 or not mask.is_contiguous():
+            raise SdpaError(5)
+        mptr = mask.data_ptr()
+    s = float("nan") if scale is None else float(scale)
+    st = (stream if stream is not None else torch.cuda.current_stream(q.device)).cuda_stream
+    rc = sdpa_forward_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), dt, q.dim(),
+                          list(q.shape), q.stride(), k.stride(), v.stride(), out.stride(),
+                          is_causal, mptr, s, st)
+    if rc != 0:
+        raise SdpaError(rc)
+    return out
+
+
+def sdpa_last_device_status(stream=None):
+    """(status, detail bits) after synchronising ``stream``."""
+    import torch
+
+    st = (stream if stream is not None else torch.cuda.current_stream()).cuda_stream
+    detail = ctypes.c_uint32(0)
+    rc = load_library().sdpa_last_device_status(ctypes.c_void_p(st) if st else None,
+                                                ctypes.byref(detail))
+    return int(rc), int(detail.value)
+
+
+def default_scale(D: int) -> float:
+    return 1.0 / math.sqrt(D)

@@ -1,0 +1,286 @@
+// sdpa_api.cpp -- C-ABI front end: argument validation, the rank-3 / rank-4
+// stride normaliser, TMA descriptor encoding and the single kernel launch.
+//
+// Rank-3 inputs [H, L, D] become [1, H, L, D] here and then follow exactly the
+// rank-4 path, so both ranks reach the same fused kernel with the same
+// per-head arithmetic -- the behaviour that "PyTorch 2.14 SDPA: rank-3 inputs
+// now take the fused kernels" (daker.dacon.io) describes as the fix for
+// rank-3 inputs silently falling back to the slow math path.  There is no
+// fallback of any kind: an unsupported layout is an error, never a slower
+// route.
+#include "../../include/sdpa.h"
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "sdpa_internal.h"
+
+namespace {
+
+constexpr uint64_t kDefaultWaitLimitNs = 1000000000ull;  // 1 s per barrier wait
+std::atomic<uint64_t> g_wait_limit_ns{kDefaultWaitLimitNs};
+std::atomic<int> g_withhold_q{0};
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn() {
+  static std::once_flag once;
+  static EncodeTiledFn fn = nullptr;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+// Per-device answer to "is this an sm_103 part?" (0 unknown, 1 yes, 2 no).
+std::atomic<int> g_device_ok[64];
+
+sdpa_status check_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SDPA_ERR_CUDA;
+  if (dev < 0 || dev >= 64) return SDPA_ERR_DEVICE;
+  int state = g_device_ok[dev].load(std::memory_order_relaxed);
+  if (state == 0) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return SDPA_ERR_CUDA;
+    state = (major == 10 && minor == 3) ? 1 : 2;
+    g_device_ok[dev].store(state, std::memory_order_relaxed);
+  }
+  return state == 1 ? SDPA_OK : SDPA_ERR_DEVICE;
+}
+
+// One operand after normalisation to rank 4: extents and element strides in
+// (B, H, L, D) order.
+struct View {
+  const void* ptr;
+  int64_t ext[4];
+  int64_t str[4];
+};
+
+// Byte span [lo, hi) touched by a 16-bit view (strides are non-negative).
+void span_of(const View& v, uintptr_t* lo, uintptr_t* hi) {
+  uint64_t last = 0;
+  for (int i = 0; i < 4; ++i) last += static_cast<uint64_t>(v.ext[i] - 1) * v.str[i];
+  *lo = reinterpret_cast<uintptr_t>(v.ptr);
+  *hi = *lo + 2 * (last + 1);
+}
+
+bool overlaps(uintptr_t a0, uintptr_t a1, uintptr_t b0, uintptr_t b1) {
+  return a0 < b1 && b0 < a1;
+}
+
+sdpa_status normalise(const void* ptr, int rank, const int64_t* shape, const int64_t* stride,
+                      View* out) {
+  out->ptr = ptr;
+  const int off = 4 - rank;  // rank 3 -> batch extent 1
+  for (int i = 0; i < 4; ++i) {
+    out->ext[i] = (i < off) ? 1 : shape[i - off];
+    out->str[i] = (i < off) ? 0 : stride[i - off];
+  }
+  return SDPA_OK;
+}
+
+sdpa_status check_layout(View* v) {
+  if ((reinterpret_cast<uintptr_t>(v->ptr) & 15u) != 0) return SDPA_ERR_LAYOUT;
+  if (v->str[3] != 1) return SDPA_ERR_LAYOUT;
+  // Extent-1 dimensions: their stride is never used; give them a harmless
+  // outermost value so the tensor map stays valid.
+  int64_t outer = 8;
+  for (int i = 0; i < 3; ++i)
+    if (v->ext[i] > 1) {
+      const int64_t s = v->str[i];
+      if (s <= 0 || (s % 8) != 0) return SDPA_ERR_LAYOUT;
+      if (s >= (int64_t(1) << 38)) return SDPA_ERR_LAYOUT;  // TMA stride < 2^40 bytes
+      if (v->ext[i] >= (int64_t(1) << 24) && s >= (int64_t(1) << 24)) return SDPA_ERR_LAYOUT;
+      if (s * v->ext[i] > outer) outer = s * v->ext[i];
+    }
+  for (int i = 0; i < 3; ++i)
+    if (v->ext[i] == 1) v->str[i] = outer;
+  return SDPA_OK;
+}
+
+// 4-D tiled TMA map over one operand.  Dimension 0 is D (contiguous); L, H and
+// B follow in increasing stride order.  The box is 64 elements of D (one
+// 128-byte swizzle atom) by 128 rows of L.  pos[] receives the map slot of
+// (L, H, B) so the kernel can place its coordinates.
+sdpa_status encode_map(const View& v, bool bf16, CUtensorMap* map, int pos[3]) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc) return SDPA_ERR_CUDA;
+  // logical outer dims: 0 = L, 1 = H, 2 = B with extents/strides from the view
+  const int64_t ext[3] = {v.ext[2], v.ext[1], v.ext[0]};
+  const int64_t str[3] = {v.str[2], v.str[1], v.str[0]};
+  int order[3] = {0, 1, 2};
+  for (int a = 0; a < 3; ++a)  // stable insertion sort by stride
+    for (int b = a + 1; b < 3; ++b)
+      if (str[order[b]] < str[order[a]]) {
+        const int t = order[a];
+        order[a] = order[b];
+        order[b] = t;
+      }
+  cuuint64_t gdim[4] = {static_cast<cuuint64_t>(v.ext[3]), 0, 0, 0};
+  cuuint64_t gstride[3];
+  cuuint32_t box[4] = {64, 1, 1, 1};
+  cuuint32_t estride[4] = {1, 1, 1, 1};
+  for (int slot = 1; slot <= 3; ++slot) {
+    const int d = order[slot - 1];
+    gdim[slot] = static_cast<cuuint64_t>(ext[d]);
+    gstride[slot - 1] = static_cast<cuuint64_t>(str[d]) * 2u;
+    box[slot] = (d == 0) ? 128u : 1u;
+    pos[d] = slot;
+  }
+  const CUresult r =
+      enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
+          const_cast<void*>(v.ptr), gdim, gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? SDPA_OK : SDPA_ERR_LAYOUT;
+}
+
+// Host-side validation shared by every entry point.  Touches no CUDA API.
+sdpa_status validate(const void* q, const void* k, const void* v, void* out, sdpa_dtype dtype,
+                     int rank, const int64_t* shape, const int64_t* q_stride,
+                     const int64_t* k_stride, const int64_t* v_stride, const int64_t* o_stride,
+                     int is_causal, const uint8_t* mask, float scale, View views[4]) {
+  if (!q || !k || !v || !out || !shape || !q_stride || !k_stride || !v_stride || !o_stride)
+    return SDPA_ERR_NULL;
+  if (rank != 3 && rank != 4) return SDPA_ERR_RANK;
+  if (dtype != SDPA_BF16 && dtype != SDPA_FP16) return SDPA_ERR_DTYPE;
+  for (int i = 0; i < rank; ++i)
+    if (shape[i] < 1) return SDPA_ERR_SHAPE;
+  const int64_t B = (rank == 4) ? shape[0] : 1;
+  const int64_t H = shape[rank - 3], L = shape[rank - 2], D = shape[rank - 1];
+  if (D != 64 && D != 128) return SDPA_ERR_SHAPE;
+  if (B * H > 0x7fffffffLL) return SDPA_ERR_SHAPE;           // grid x
+  if ((L + 127) / 128 > 65535) return SDPA_ERR_SHAPE;        // grid y
+  const void* ptrs[4] = {q, k, v, out};
+  const int64_t* strides[4] = {q_stride, k_stride, v_stride, o_stride};
+  for (int t = 0; t < 4; ++t) {
+    normalise(ptrs[t], rank, shape, strides[t], &views[t]);
+    const sdpa_status s = check_layout(&views[t]);
+    if (s != SDPA_OK) return s;
+  }
+  if (is_causal && mask) return SDPA_ERR_ARG;
+  if (std::isinf(scale)) return SDPA_ERR_ARG;
+  // out must not alias any input (the kernel reads inputs while writing out)
+  uintptr_t o0, o1;
+  View raw_out;
+  normalise(out, rank, shape, o_stride, &raw_out);
+  span_of(raw_out, &o0, &o1);
+  for (int t = 0; t < 3; ++t) {
+    View raw;
+    normalise(ptrs[t], rank, shape, strides[t], &raw);
+    uintptr_t a0, a1;
+    span_of(raw, &a0, &a1);
+    if (overlaps(o0, o1, a0, a1)) return SDPA_ERR_ARG;
+  }
+  if (mask) {
+    const uintptr_t m0 = reinterpret_cast<uintptr_t>(mask);
+    const uintptr_t m1 = m0 + static_cast<uintptr_t>(L) * static_cast<uintptr_t>(L);
+    if (overlaps(o0, o1, m0, m1)) return SDPA_ERR_ARG;
+  }
+  return SDPA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+sdpa_status sdpa_forward(const void* q, const void* k, const void* v, void* out,
+                         sdpa_dtype dtype, int rank, const int64_t* shape,
+                         const int64_t* q_stride, const int64_t* k_stride,
+                         const int64_t* v_stride, const int64_t* o_stride, int is_causal,
+                         const uint8_t* mask, float scale, void* stream) {
+  View views[4];
+  sdpa_status s = validate(q, k, v, out, dtype, rank, shape, q_stride, k_stride, v_stride,
+                           o_stride, is_causal, mask, scale, views);
+  if (s != SDPA_OK) return s;
+  s = check_device();
+  if (s != SDPA_OK) return s;
+
+  const bool bf16 = (dtype == SDPA_BF16);
+  const int64_t B = views[0].ext[0], H = views[0].ext[1], L = views[0].ext[2],
+                D = views[0].ext[3];
+  sdpa_impl::FwdParams p;
+  std::memset(&p, 0, sizeof(p));
+  if ((s = encode_map(views[0], bf16, &p.tm_q, p.pos_q)) != SDPA_OK) return s;
+  if ((s = encode_map(views[1], bf16, &p.tm_k, p.pos_k)) != SDPA_OK) return s;
+  if ((s = encode_map(views[2], bf16, &p.tm_v, p.pos_v)) != SDPA_OK) return s;
+  p.out = out;
+  p.o_sb = views[3].str[0];
+  p.o_sh = views[3].str[1];
+  p.o_sl = views[3].str[2];
+  p.mask = mask;
+  p.B = static_cast<int>(B);
+  p.H = static_cast<int>(H);
+  p.L = static_cast<int>(L);
+  p.n_tiles = static_cast<int>((L + 127) / 128);
+  const double sc = std::isnan(scale) ? 1.0 / std::sqrt(static_cast<double>(D))
+                                      : static_cast<double>(scale);
+  p.scale_log2 = static_cast<float>(sc * 1.4426950408889634);  // log2(e)
+  p.mask_vec16 = (mask && (L % 16) == 0 && (reinterpret_cast<uintptr_t>(mask) & 15u) == 0);
+  p.debug_withhold_q = g_withhold_q.load(std::memory_order_relaxed);
+  p.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
+
+  const int mode = is_causal ? sdpa_impl::kMaskCausal
+                             : (mask ? sdpa_impl::kMaskExplicit : sdpa_impl::kMaskNone);
+  const cudaError_t e = sdpa_impl::launch_forward(p, static_cast<int>(D), mode, bf16,
+                                                  static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;
+}
+
+const char* sdpa_status_string(sdpa_status status) {
+  switch (status) {
+    case SDPA_OK: return "SDPA_OK";
+    case SDPA_ERR_NULL: return "SDPA_ERR_NULL: a required pointer is NULL";
+    case SDPA_ERR_RANK: return "SDPA_ERR_RANK: rank must be 3 or 4";
+    case SDPA_ERR_SHAPE: return "SDPA_ERR_SHAPE: D must be 64 or 128 and every extent >= 1";
+    case SDPA_ERR_DTYPE: return "SDPA_ERR_DTYPE: dtype must be SDPA_BF16 or SDPA_FP16";
+    case SDPA_ERR_LAYOUT:
+      return "SDPA_ERR_LAYOUT: inner stride must be 1, other strides positive multiples of 8 "
+             "elements, pointers 16-byte aligned";
+    case SDPA_ERR_ARG:
+      return "SDPA_ERR_ARG: causal with mask, infinite scale, or out overlapping an input";
+    case SDPA_ERR_CUDA: return "SDPA_ERR_CUDA: CUDA runtime or driver error";
+    case SDPA_ERR_DEVICE_TIMEOUT:
+      return "SDPA_ERR_DEVICE_TIMEOUT: a kernel barrier wait ran out of time";
+    case SDPA_ERR_DEVICE: return "SDPA_ERR_DEVICE: the current device is not sm_103";
+  }
+  return "SDPA_UNKNOWN_STATUS";
+}
+
+sdpa_status sdpa_last_device_status(void* stream, uint32_t* detail) {
+  unsigned int st = 0;
+  if (sdpa_impl::read_and_clear_device_status(static_cast<cudaStream_t>(stream), &st) !=
+      cudaSuccess)
+    return SDPA_ERR_CUDA;
+  if (detail) *detail = st;
+  return st == 0 ? SDPA_OK : SDPA_ERR_DEVICE_TIMEOUT;
+}
+
+int sdpa_version(void) { return 100; }
+
+void sdpa_debug_set_wait_limit_ns(uint64_t ns) {
+  g_wait_limit_ns.store(ns == 0 ? kDefaultWaitLimitNs : ns, std::memory_order_relaxed);
+}
+
+void sdpa_debug_withhold_q_load(int enable) {
+  g_withhold_q.store(enable ? 1 : 0, std::memory_order_relaxed);
+}
+
+}  // extern "C"

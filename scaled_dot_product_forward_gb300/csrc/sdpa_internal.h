@@ -1,0 +1,38 @@
+// sdpa_internal.h -- shared between the C-ABI front end and the kernel
+// translation unit.  Not part of the public interface.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace sdpa_impl {
+
+// Kernel arguments; passed by value as a __grid_constant__ parameter so the
+// TMA descriptors live in parameter space (no device allocation per call).
+struct FwdParams {
+  CUtensorMap tm_q;  // 4-D maps over (D, and L/H/B in stride order); box 64 x 128 rows
+  CUtensorMap tm_k;
+  CUtensorMap tm_v;
+  void* out;          // [B, H, L, D] with element strides below (inner stride 1)
+  int64_t o_sb, o_sh, o_sl;
+  const uint8_t* mask;  // [L, L] row-major bytes, nonzero = removed; null unless mask mode
+  int B, H, L;
+  int n_tiles;          // ceil(L / 128)
+  float scale_log2;     // scale * log2(e)
+  int pos_q[3], pos_k[3], pos_v[3];  // tensor-map coordinate slot (1..3) of L, H, B
+  int mask_vec16;       // 1: mask rows may be read as 16-byte vectors (L % 16 == 0, aligned)
+  int debug_withhold_q; // test hook: 1 = never load Q, so every consumer wait runs out
+  uint64_t wait_limit_ns;  // bound on any single barrier wait
+};
+
+enum MaskMode : int { kMaskNone = 0, kMaskCausal = 1, kMaskExplicit = 2 };
+
+// Launches the fused forward kernel for (head_dim, mask mode, dtype) on
+// `stream`.  Returns the CUDA error of the launch.
+cudaError_t launch_forward(const FwdParams& p, int head_dim, int mask_mode, bool bf16,
+                           cudaStream_t stream);
+
+// Reads and clears the device status word (nonzero = a barrier wait timed out).
+cudaError_t read_and_clear_device_status(cudaStream_t stream, unsigned int* status);
+
+}  // namespace sdpa_impl

@@ -1,0 +1,148 @@
+"""Host-side tests of the C ABI (no GPU needed): the library builds for
+sm_103a, loads, exports every function the header declares, and rejects bad
+arguments with the documented status codes before touching CUDA."""
+import ctypes
+import math
+import os
+import re
+
+import pytest
+
+from scaled_dot_product_forward_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "sdpa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    import scaled_dot_product_forward_gb300 as sdpa
+    return sdpa
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return re.findall(r"SDPA_API\s+[\w\s\*]+?\b(\w+)\s*\(", text)
+
+
+def test_header_declares_entry_points():
+    names = declared_functions()
+    for n in ["sdpa_forward", "sdpa_status_string", "sdpa_last_device_status", "sdpa_version"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    cdll = ctypes.CDLL(_build.LIB_PATH)
+    for name in declared_functions():
+        assert hasattr(cdll, name), f"{name} declared in sdpa.h but not exported"
+
+
+def test_only_declared_symbols_are_exported():
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", _build.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    ours = {s for s in exported if "sdpa" in s}
+    assert ours == set(declared_functions())
+
+
+def test_status_strings(lib):
+    for code, name in lib.STATUS.items():
+        assert lib.sdpa_status_string(code).startswith(name)
+    assert lib.sdpa_status_string(99) == "SDPA_UNKNOWN_STATUS"
+    assert lib.sdpa_version() == 100
+
+
+# Fake, well-aligned device addresses: validation only does arithmetic on them.
+Q, K, V, O, M = 0x10000000, 0x20000000, 0x30000000, 0x40000000, 0x50000000
+
+
+def contiguous(shape):
+    st, acc = [], 1
+    for e in reversed(shape):
+        st.append(acc)
+        acc *= e
+    return list(reversed(st))
+
+
+def call(lib, q=Q, k=K, v=V, o=O, dtype=0, rank=4, shape=(2, 3, 256, 64), strides=None,
+         causal=1, mask=None, scale=float("nan")):
+    st = strides or contiguous(shape)
+    return lib.sdpa_forward_raw(q, k, v, o, dtype, rank, list(shape), st, st, st, st, causal,
+                                mask, scale, 0)
+
+
+def test_null_pointers(lib):
+    assert call(lib, q=0) == 1
+    assert call(lib, o=0) == 1
+    c = ctypes.CDLL(_build.LIB_PATH)
+    c.sdpa_forward.restype = ctypes.c_int
+    assert c.sdpa_forward(ctypes.c_void_p(Q), ctypes.c_void_p(K), ctypes.c_void_p(V),
+                          ctypes.c_void_p(O), 0, 4, None, None, None, None, None, 1, None,
+                          ctypes.c_float(1.0), None) == 1
+
+
+def test_rank(lib):
+    assert call(lib, rank=2, shape=(256, 64)) == 2
+    assert call(lib, rank=5, shape=(1, 2, 3, 256, 64)) == 2
+
+
+def test_dtype(lib):
+    assert call(lib, dtype=2) == 4
+
+
+@pytest.mark.parametrize("shape", [(2, 3, 256, 96), (2, 3, 256, 32), (2, 3, 0, 64),
+                                   (0, 3, 256, 64), (2, 3, 65536 * 128, 64)])
+def test_shape(lib, shape):
+    assert call(lib, shape=shape) == 3
+
+
+def test_layout(lib):
+    shape = (2, 3, 256, 64)
+    st = contiguous(shape)
+    assert call(lib, strides=st[:3] + [2]) == 5                    # inner stride != 1
+    assert call(lib, strides=[st[0], st[1], 68, 1]) == 5           # row stride not 16-byte multiple
+    assert call(lib, q=Q + 8) == 5                                 # pointer not 16-byte aligned
+    assert call(lib, strides=[st[0], 0, st[2], 1]) == 5            # broadcast head stride
+    assert call(lib, strides=[st[0], st[1], -64, 1]) == 5          # negative stride
+
+
+def test_args(lib):
+    assert call(lib, causal=1, mask=M) == 6                        # causal and mask together
+    assert call(lib, o=Q + 512) == 6                               # out overlaps q
+    assert call(lib, scale=math.inf) == 6
+    L = 256
+    assert call(lib, causal=0, mask=O + 2 * 2 * 3 * L * 64 - 64) == 6   # mask overlaps out
+
+
+def test_rank3_shape_accepted_by_validation(lib):
+    """A rank-3 [H, L, D] call passes validation; without a GPU it then fails
+    loudly with SDPA_ERR_CUDA (there is no CPU fallback)."""
+    import torch
+    rc = call(lib, rank=3, shape=(4, 128, 64))
+    if torch.cuda.is_available():
+        pytest.skip("a real device is present; validation-only check")
+    assert rc == 7
+
+
+def test_permuted_view_accepted_by_validation(lib):
+    import torch
+    # [B, L, H, D] buffer viewed as [B, H, L, D]
+    B, H, L, D = 2, 3, 256, 64
+    st = [L * H * D, D, H * D, 1]
+    rc = call(lib, shape=(B, H, L, D), strides=st)
+    if torch.cuda.is_available():
+        pytest.skip("a real device is present; validation-only check")
+    assert rc == 7
+
+
+def test_python_wrapper_type_checks(lib):
+    import torch
+    x = torch.zeros(1, 2, 8, 64, dtype=torch.float32)
+    with pytest.raises(lib.SdpaError):
+        lib.sdpa_forward(x, x, x, is_causal=True)
+    y = torch.zeros(1, 2, 8, 64, dtype=torch.bfloat16)
+    z = torch.zeros(1, 2, 8, 64, dtype=torch.float16)
+    with pytest.raises(lib.SdpaError):
+        lib.sdpa_forward(y, z, y, is_causal=True)
