@@ -1,0 +1,388 @@
+"""Benchmark: fused causal SDPA forward on one GB300, plus the fp64 oracle's
+CPU baseline.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 3] [--impl reference]
+
+One step = one fused forward (one kernel launch) over the workload's whole
+batch.  Default workload: causal [B=4, H=32, L=4096, D=128] bf16, q/k/v drawn
+N(0,1)*0.5 from fixed seeds.  Prints ONE JSON line (rank 0).
+
+value        algorithmic TFLOP/s (causal: 2*B*H*L^2*D per forward) with inputs
+             resident in HBM, K steps timed with CUDA events on the launch
+             stream; q, k, v, out total 537 MB > the 129 MB L2, so no flush.
+e2e          the same metric through the same C-ABI call, with pinned host
+             buffers: the H2D copy of q, k, v and the D2H copy of out are inside
+             the timed region every step.
+roofline     achieved = algorithmic FLOPs per launch / mean per-launch kernel
+             time (CUDA events around each launch in the timed region); peak =
+             the measured dense bf16 GEMM rate (burst) of this GPU model.
+cpu_baseline the fp64 oracle on the host cores, on a bounded sample of query
+             rows of the same workload, in the same unit.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "causal SDPA fwd TFLOP/s at B4·H32·L4096·D128 bf16; % of GB300 tensor peak"
+UNIT = "TFLOP/s"
+FALLBACK_BF16_TFLOPS = 1900.0
+KERNEL_SOURCES = ["scaled_dot_product_forward_gb300/csrc/sdpa_fwd_sm103a.cu",
+                  "scaled_dot_product_forward_gb300/csrc/ptx.cuh"]
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return float(pk["bf16_tflops"]), float(pk.get("hbm_gbs", 0.0)), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_BF16_TFLOPS, 6800.0, "fallback"
+
+
+def load_traffic(workload_id: int):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            t = json.load(f)
+    except (OSError, ValueError):
+        return None
+    entry = t.get(str(workload_id))
+    if not entry or entry.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    return entry.get("dram_bytes_per_launch")
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi samples (200 ms) over the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=5)
+        sms, maxes, reasons, powers = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sms.append(float(parts[1]))
+                maxes.append(float(parts[2]))
+                powers.append(float(parts[3]))
+            except ValueError:
+                continue
+            for n, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(n)
+        if not sms:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sms), "sm_max_mhz": max(maxes),
+                "reasons": sorted(reasons), "samples": len(sms),
+                "power_w_max": max(powers) if powers else None}
+
+
+# --------------------------------------------------------- CPU (oracle) leg
+class OracleSampler:
+    """Times the fp64 oracle on random query rows of one head of workload
+    ``w`` (the operands are generated and widened once)."""
+
+    def __init__(self, w):
+        import numpy as np
+        import torch
+
+        import oracle
+        import sdpa_inputs
+
+        self.w = w
+        q, k, v, mask = sdpa_inputs.make(w)
+        if w.rank == 3:
+            q, k, v = q[None], k[None], v[None]
+        self.q, self.k, self.v = (x[:1, :1].to(torch.float64).numpy() for x in (q, k, v))
+        self.mask = None if mask is None else (mask.numpy() != 0).astype(np.uint8)
+        self.oracle = oracle
+        self.rate = None  # rows per second
+
+    def _flops(self, rows):
+        w = self.w
+        if w.is_causal:
+            return float(sum(4.0 * w.D * (i + 1) for i in rows[:, 2]))
+        return float(len(rows) * 4.0 * w.D * w.L)
+
+    def run(self, budget_s: float, seed: int = 0):
+        """(algorithmic FLOPs, seconds, rows) for about ``budget_s`` of work."""
+        import numpy as np
+        g = np.random.default_rng(seed)
+        if self.rate is None:
+            n0 = max(8, self.oracle.num_threads())
+            rows = np.zeros((n0, 3), dtype=np.int64)
+            rows[:, 2] = g.integers(0, self.w.L, size=n0)
+            t0 = time.perf_counter()
+            self.oracle.sdpa_rows(self.q, self.k, self.v, rows, mask=self.mask,
+                                  is_causal=self.w.is_causal, scale=self.w.scale)
+            self.rate = n0 / max(time.perf_counter() - t0, 1e-6)
+        n = max(1, int(self.rate * budget_s))
+        rows = np.zeros((n, 3), dtype=np.int64)
+        rows[:, 2] = g.integers(0, self.w.L, size=n)
+        t0 = time.perf_counter()
+        self.oracle.sdpa_rows(self.q, self.k, self.v, rows, mask=self.mask,
+                              is_causal=self.w.is_causal, scale=self.w.scale)
+        return self._flops(rows), time.perf_counter() - t0, n
+
+    @property
+    def cores(self):
+        return self.oracle.num_threads()
+
+
+# ---------------------------------------------------------------- GPU leg
+def gpu_leg(args, w, rank, world):
+    import torch
+
+    import scaled_dot_product_forward_gb300 as sdpa
+    import sdpa_inputs
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    sdpa.load_library()
+    q, k, v, mask = sdpa_inputs.make(w)
+    qd, kd, vd = (x.to(dev) for x in (q, k, v))
+    md = mask.to(dev) if mask is not None else None
+    out = torch.empty_like(qd)
+    stream = torch.cuda.Stream(dev)
+    flops = w.flops()
+
+    def step():
+        sdpa.sdpa_forward(qd, kd, vd, out, is_causal=w.is_causal, mask=md, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    stream.synchronize()
+    rc, detail = sdpa.sdpa_last_device_status(stream)
+    if rc != 0:
+        raise RuntimeError(f"warm-up reported {sdpa.sdpa_status_string(rc)} ({detail:#x})")
+
+    # --- timed region: K launches, an event pair around each one
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    t_begin, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(dev.index)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    time.sleep(0.3)  # let the sampler start before the work
+    t_begin.record(stream)
+    for i in range(args.steps):
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    if world > 1:
+        torch.distributed.barrier()
+    total_ms = t_begin.elapsed_time(t_end)
+    per_launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    rc, detail = sdpa.sdpa_last_device_status(stream)
+    if rc != 0:
+        raise RuntimeError(f"timed region reported {sdpa.sdpa_status_string(rc)} ({detail:#x})")
+
+    # --- end to end through host buffers
+    e2e_steps = max(3, min(args.steps, args.e2e_steps))
+    hq, hk, hv = (x.pin_memory() for x in (q, k, v))
+    hout = torch.empty(q.shape, dtype=q.dtype).pin_memory()
+    hm = mask.pin_memory() if mask is not None else None
+
+    def e2e_step():
+        qd.copy_(hq, non_blocking=True)
+        kd.copy_(hk, non_blocking=True)
+        vd.copy_(hv, non_blocking=True)
+        if hm is not None:
+            md.copy_(hm, non_blocking=True)
+        step()
+        hout.copy_(out, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            e2e_step()
+        stream.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        e1.record(stream)
+    stream.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv)) + (
+        hm.numel() if hm is not None else 0)
+    d2h = hout.numel() * hout.element_size()
+    return dict(total_ms=total_ms, per_launch_ms=per_launch_ms, clocks=clk, e2e_ms=e2e_ms,
+                h2d=h2d, d2h=d2h, flops=flops)
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64,
+                     device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-budget-s", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    import sdpa_inputs
+    w = sdpa_inputs.WORKLOADS[args.workload]
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    config = {"workload": w.name, "B": w.B, "H": w.H, "L": w.L, "D": w.D,
+              "is_causal": w.is_causal, "mask": w.p_masked is not None,
+              "rank": w.rank, "scale": "1/sqrt(D)",
+              "l2": "no flush: q, k, v, out total %.0f MB > 129 MB L2" % (
+                  4 * w.heads * w.L * w.D * 2 / 1e6)}
+    dtype = "bf16" if "bf16" in w.name else "fp16"
+
+    if args.impl == "reference":
+        # The reference arm is the fp64 oracle on the host cores.
+        if rank != 0:
+            return 0
+        per_step = max(0.02, 120.0 / (args.steps + args.warmup))
+        sampler = OracleSampler(w)
+        for i in range(args.warmup):
+            sampler.run(per_step / 4, seed=1000 + i)
+        tf, tt, rows = 0.0, 0.0, 0
+        for i in range(args.steps):
+            f, t, n = sampler.run(per_step, seed=i + 1)
+            tf, tt, rows = tf + f, tt + t, rows + n
+        cores = sampler.cores
+        val = tf / tt / 1e12
+        line = {"impl": "reference", "metric": METRIC, "value": val, "unit": UNIT,
+                "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": 1e3 * tt / args.steps, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": config,
+                "cpu_baseline": {"value": val, "unit": UNIT, "cores": cores, "kind": "oracle",
+                                 "sample": f"{rows} query rows of head (0,0) of the workload, "
+                                           f"{args.steps} steps"},
+                "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return 0
+
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group(backend="nccl")
+
+    r = gpu_leg(args, w, rank, world)
+    total_ms = max_over_ranks(r["total_ms"], world)
+    ms_per_step = total_ms / args.steps
+    value = world * r["flops"] / (ms_per_step * 1e-3) / 1e12
+    mean_launch_ms = statistics.fmean(r["per_launch_ms"])
+    achieved = r["flops"] / (mean_launch_ms * 1e-3) / 1e12
+    peak, _, peak_kind = load_peaks()
+    traffic = load_traffic(args.workload)
+    e2e_ms = max_over_ranks(r["e2e_ms"], world)
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": dtype, "data": "synthetic",
+            "config": config,
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
+                         "unit": UNIT, "frac": achieved / peak,
+                         "peak_source": f"{peak_kind} dense bf16 (burst)",
+                         "traffic": traffic,
+                         "alg_flops_per_launch": r["flops"],
+                         "mean_launch_ms": mean_launch_ms},
+            "e2e": {"value": world * r["flops"] / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+                    "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"],
+                    "ms_per_step": e2e_ms},
+            "gpu_launches": args.steps,
+            "clocks": r["clocks"]}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        sampler = OracleSampler(w)
+        f, t, rows = sampler.run(args.cpu_budget_s)
+        cores = sampler.cores
+        line["cpu_baseline"] = {"value": f / t / 1e12, "unit": UNIT, "cores": cores,
+                                "kind": "oracle",
+                                "sample": f"{rows} random query rows of head (0,0), "
+                                          f"algorithmic FLOPs of those rows, {t:.1f} s"}
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -166,8 +166,8 @@ sdpa_status validate(const void* q, const void* k, const void* v, void* out, sdp
   const int64_t B = (rank == 4) ? shape[0] : 1;
   const int64_t H = shape[rank - 3], L = shape[rank - 2], D = shape[rank - 1];
   if (D != 64 && D != 128) return SDPA_ERR_SHAPE;
-  if (B * H > 0x7fffffffLL) return SDPA_ERR_SHAPE;           // grid x
-  if ((L + 127) / 128 > 65535) return SDPA_ERR_SHAPE;        // grid y
+  if (L > 0x7fffffffLL - 127) return SDPA_ERR_SHAPE;
+  if (B * H > 0x7fffffffLL / ((L + 127) / 128)) return SDPA_ERR_SHAPE;  // one CTA per tile
   const void* ptrs[4] = {q, k, v, out};
   const int64_t* strides[4] = {q_stride, k_stride, v_stride, o_stride};
   for (int t = 0; t < 4; ++t) {

@@ -8,7 +8,8 @@
 // query tile with an online softmax, so the [seq, seq] score matrix never
 // reaches HBM -- but built for Blackwell:
 //
-//   * one CTA per (batch*head, 128-row query tile), heaviest causal tiles first;
+//   * one CTA per (batch*head, 128-row query tile); a head's tiles are adjacent
+//     in launch order (heaviest causal tile first) so K/V stay in L2;
 //   * warp 0 (one lane) streams Q once and a ring of K/V tiles with TMA
 //     (128-byte swizzled boxes of 64 x 128 elements) into shared memory;
 //   * warp 1 (one lane) issues tcgen05.mma: S_j = Q K_j^T into one of two TMEM
@@ -60,7 +61,7 @@ struct Layout {
   static constexpr int kChunks = D / 64;               // 128-byte swizzle atoms along D
   static constexpr int kChunkBytes = kBlockM * 128;    // one 128-row x 64-element box
   static constexpr int kTileBytes = kChunks * kChunkBytes;
-  static constexpr int kStages = (D == 64) ? 4 : 2;    // K/V ring depth
+  static constexpr int kStages = (D == 64) ? 4 : 3;    // K/V ring depth
   static constexpr int kQ = 0;
   static constexpr int kK = kQ + kTileBytes;
   static constexpr int kV = kK + kStages * kTileBytes;
@@ -75,12 +76,15 @@ struct Barriers {
   uint64_t p_ready[2];
   uint64_t pv_done;
   uint64_t fin;
-  uint64_t kv_full[4];
+  uint64_t k_full[4];
+  uint64_t v_full[4];
   uint64_t kv_empty[4];
   uint32_t tmem_base;
   uint32_t abort_flag;
 };
 static_assert(sizeof(Barriers) <= 256, "barrier block too large");
+static_assert(Layout<128>::kTotal <= 227 * 1024, "shared memory over the per-CTA limit");
+static_assert(Layout<64>::kTotal <= 227 * 1024, "shared memory over the per-CTA limit");
 
 // Bounded wait on one barrier phase.  Returns false when the wait gave up:
 // either another role already raised the CTA abort flag (honour_abort), or
@@ -150,10 +154,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int bh = blockIdx.x;
+  // Launch order walks one head's query tiles (heaviest first) before the
+  // next head, so the CTAs resident at any time share a few heads' K/V in L2.
+  const int bh = static_cast<int>(blockIdx.x / static_cast<unsigned>(p.n_tiles));
   const int batch = bh / p.H;
   const int head = bh - batch * p.H;
-  const int q_tile = p.n_tiles - 1 - static_cast<int>(blockIdx.y);  // heaviest first
+  const int q_tile = p.n_tiles - 1 - static_cast<int>(blockIdx.x - bh * p.n_tiles);
   const int n_kv = (MODE == sdpa_impl::kMaskCausal) ? (q_tile + 1) : p.n_tiles;
   const uint64_t limit = p.wait_limit_ns;
 
@@ -167,7 +173,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->fin, 1);
 #pragma unroll
     for (int s = 0; s < Lay::kStages; ++s) {
-      mbar_init(&bars->kv_full[s], 1);
+      mbar_init(&bars->k_full[s], 1);
+      mbar_init(&bars->v_full[s], 1);
       mbar_init(&bars->kv_empty[s], 1);
     }
     bars->abort_flag = 0;
@@ -207,22 +214,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (use > 0 &&
             !wait_phase(&bars->kv_empty[s], (use - 1) & 1, bars, limit, kSiteKvEmpty))
           break;
-        mbar_arrive_expect_tx(&bars->kv_full[s], 2 * Lay::kTileBytes);
+        mbar_arrive_expect_tx(&bars->k_full[s], Lay::kTileBytes);
 #pragma unroll
-        for (int c = 0; c < Lay::kChunks; ++c) {
-          tma_tile(sK + s * Lay::kTileBytes + c * Lay::kChunkBytes, &p.tm_k, &bars->kv_full[s],
+        for (int c = 0; c < Lay::kChunks; ++c)
+          tma_tile(sK + s * Lay::kTileBytes + c * Lay::kChunkBytes, &p.tm_k, &bars->k_full[s],
                    c * 64, j * kBlockN, head, batch, p.pos_k);
-          tma_tile(sV + s * Lay::kTileBytes + c * Lay::kChunkBytes, &p.tm_v, &bars->kv_full[s],
+        mbar_arrive_expect_tx(&bars->v_full[s], Lay::kTileBytes);
+#pragma unroll
+        for (int c = 0; c < Lay::kChunks; ++c)
+          tma_tile(sV + s * Lay::kTileBytes + c * Lay::kChunkBytes, &p.tm_v, &bars->v_full[s],
                    c * 64, j * kBlockN, head, batch, p.pos_v);
-        }
         issued[s] = use + 1;
       }
       // Drain: every load issued must have landed before shared memory is
       // released (only matters when a wait gave up).
 #pragma unroll
       for (int s = 0; s < Lay::kStages; ++s)
-        if (issued[s] > 0)
-          wait_phase(&bars->kv_full[s], (issued[s] - 1) & 1, bars, limit, kSiteDrain, false);
+        if (issued[s] > 0) {
+          wait_phase(&bars->k_full[s], (issued[s] - 1) & 1, bars, limit, kSiteDrain, false);
+          wait_phase(&bars->v_full[s], (issued[s] - 1) & 1, bars, limit, kSiteDrain, false);
+        }
       if (!p.debug_withhold_q)
         wait_phase(&bars->q_full, 0, bars, limit, kSiteDrain, false);
     }
@@ -239,10 +250,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       // O += P_jp V_jp, with P_jp read from the TMEM score buffer it replaced.
       auto issue_pv = [&](int jp) -> bool {
         const int bp = jp & 1;
+        const int sp = jp % Lay::kStages;
+        if (!wait_phase(&bars->v_full[sp], (jp / Lay::kStages) & 1, bars, limit, kSiteKvFull))
+          return false;
         if (!wait_phase(&bars->p_ready[bp], (jp >> 1) & 1, bars, limit, kSitePReady))
           return false;
         tc_fence_after();
-        const int sp = jp % Lay::kStages;
         const uint32_t tP = bp ? tS1 : tS0;
 #pragma unroll
         for (int kk = 0; kk < kBlockN / 16; ++kk) {
@@ -262,7 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         for (int j = 0; j < n_kv && ok; ++j) {
           const int s = j % Lay::kStages;
-          if (!wait_phase(&bars->kv_full[s], (j / Lay::kStages) & 1, bars, limit,
+          if (!wait_phase(&bars->k_full[s], (j / Lay::kStages) & 1, bars, limit,
                           kSiteKvFull)) {
             ok = false;
             break;
@@ -480,7 +493,7 @@ cudaError_t launch_one(const sdpa_impl::FwdParams& p, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  dim3 grid(static_cast<unsigned>(p.B * p.H), static_cast<unsigned>(p.n_tiles));
+  dim3 grid(static_cast<unsigned>(p.n_tiles) * static_cast<unsigned>(p.B * p.H));
   kern<<<grid, kThreads, smem, stream>>>(p);
   return cudaGetLastError();
 }
