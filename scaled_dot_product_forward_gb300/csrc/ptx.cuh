@@ -192,6 +192,18 @@ __device__ __forceinline__ void tmem_st_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// Per-warpgroup register budget (all four warps of a warpgroup execute the
+// same instruction).  The increases must fit in what the decreases release
+// from the block's launch-time allocation, or the increasing warps wait.
+template <uint32_t N>
+__device__ __forceinline__ void regs_decrease() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void regs_increase() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // --------------------------------------------------------------- math
 // Hardware base-2 exponential (MUFU); ex2(-inf) = +0.
 __device__ __forceinline__ float ex2(float x) {

@@ -11,6 +11,7 @@
 #include "../../include/sdpa.h"
 
 #include <atomic>
+#include <cfloat>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -233,6 +234,11 @@ sdpa_status sdpa_forward(const void* q, const void* k, const void* v, void* out,
   const double sc = std::isnan(scale) ? 1.0 / std::sqrt(static_cast<double>(D))
                                       : static_cast<double>(scale);
   p.scale_log2 = static_cast<float>(sc * 1.4426950408889634);  // log2(e)
+  // A zero scale makes every admissible weight exp(0) = 1.  The kernel needs
+  // a nonzero multiplier (a removed score is an infinity that must map to
+  // -inf), so it gets the smallest normal float instead: every finite score
+  // times it rounds the exponent to 0 and the weights are exactly 1.0f.
+  if (p.scale_log2 == 0.0f) p.scale_log2 = std::signbit(sc) ? -FLT_MIN : FLT_MIN;
   p.mask_vec16 = (mask && (L % 16) == 0 && (reinterpret_cast<uintptr_t>(mask) & 15u) == 0);
   p.debug_withhold_q = g_withhold_q.load(std::memory_order_relaxed);
   p.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);

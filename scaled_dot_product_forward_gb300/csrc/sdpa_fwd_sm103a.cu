@@ -4,22 +4,27 @@
 // boolean masking) V: the five-step attention of "Profiling attention in
 // PyTorch: kernels, backends and where the time goes" (news.bpdata.com),
 // section "Naiv causal attention", evaluated the way that page's "Flash
-// backend" section describes -- tiles of K and V streamed past an on-chip
-// query tile with an online softmax, so the [seq, seq] score matrix never
-// reaches HBM -- but built for Blackwell:
+// backend" section describes -- tiles of K and V streamed past on-chip query
+// tiles with an online softmax, so the [seq, seq] score matrix never reaches
+// HBM -- but built for Blackwell:
 //
-//   * one CTA per (batch*head, 128-row query tile); a head's tiles are adjacent
-//     in launch order (heaviest causal tile first) so K/V stay in L2;
-//   * warp 0 (one lane) streams Q once and a ring of K/V tiles with TMA
-//     (128-byte swizzled boxes of 64 x 128 elements) into shared memory;
-//   * warp 1 (one lane) issues tcgen05.mma: S_j = Q K_j^T into one of two TMEM
-//     score buffers, and O += P_j V_j with P read straight from TMEM;
-//   * warps 4..7 (one query row per thread, TMEM lane = row) load S_j from
-//     TMEM, apply scale, causal / explicit / ragged-tail masks and the online
-//     softmax in registers (a whole score row lives in one thread, so row max
-//     and row sum need no shuffles), write P_j back over S_j as 16-bit pairs,
-//     rescale O in TMEM only when the running maximum grows by more than 2^8,
-//     and finally write O / l.
+//   * one CTA per pair of adjacent 128-row query tiles (A = rows 256m..,
+//     B = rows 256m+128..) of one (batch, head); a head's pairs are adjacent
+//     in launch order, heaviest causal pair first, so K/V stay in L2;
+//   * warp 0 (one lane) streams Q_A, Q_B once and rings of K and V tiles
+//     with TMA (128-byte swizzled boxes of 64 x 128 elements), K and V with
+//     their own full/empty barriers;
+//   * warp 1 (one lane) issues tcgen05.mma in the order
+//       S_A(0) S_B(0) | PV_A(0) S_A(1) PV_B(0) S_B(1) | PV_A(1) S_A(2) ...
+//     so that while one softmax warpgroup works on its tile the tensor core
+//     is busy with the other tile's products; S = Q K^T lands in TMEM, and
+//     P (16-bit, written over S) is read from TMEM by O += P V;
+//   * warpgroup 1 owns tile A, warpgroup 2 tile B: one query row per thread
+//     (TMEM lane = row), so row max and row sum are in-thread tree
+//     reductions with no shuffles; scale, causal / explicit / ragged-tail
+//     masks and the online softmax happen in registers, O is rescaled in
+//     TMEM only when the running maximum grows by more than 2^8, and the
+//     epilogue writes O / l.
 //
 // Safe softmax: a row with no admissible key ends with l = 0 and is written
 // as zeros, as the math backend's _safe_softmax does (same page, "Math
@@ -42,18 +47,28 @@ namespace {
 
 constexpr int kBlockM = 128;   // query rows per tile (TMEM lanes)
 constexpr int kBlockN = 128;   // keys per tile
-constexpr int kThreads = 256;  // 8 warps: TMA, MMA, 2 idle, 4 softmax
+constexpr int kTilesPerCta = 2;
+constexpr int kThreads = 384;  // WG0: TMA warp, MMA warp, 2 spare; WG1: tile A; WG2: tile B
+// Register split: the launch reserves kLaunchRegs per thread (the cap that
+// __launch_bounds__(384, 1) implies); WG0 gives registers back, the two
+// softmax warpgroups take them.  128*56 + 256*224 == 384*168.
+constexpr uint32_t kLaunchRegs = 168;
+constexpr uint32_t kRegsControl = 56;
+constexpr uint32_t kRegsSoftmax = 224;
+static_assert(128 * kRegsControl + 256 * kRegsSoftmax <= kThreads * kLaunchRegs,
+              "register split exceeds the launch allocation");
 constexpr float kRescaleLog2 = 8.0f;  // rescale O only when max grows by > 2^8
 constexpr uint32_t kTmemCols = 512;
 
 enum WaitSite : unsigned int {
   kSiteQFull = 1u << 1,
-  kSiteKvFull = 1u << 2,
-  kSiteKvEmpty = 1u << 3,
+  kSiteKFull = 1u << 2,
+  kSiteEmpty = 1u << 3,
   kSiteSFull = 1u << 4,
   kSitePReady = 1u << 5,
-  kSitePvDone = 1u << 6,
+  kSiteODone = 1u << 6,
   kSiteDrain = 1u << 7,
+  kSiteVFull = 1u << 8,
 };
 
 template <int D>
@@ -61,30 +76,33 @@ struct Layout {
   static constexpr int kChunks = D / 64;               // 128-byte swizzle atoms along D
   static constexpr int kChunkBytes = kBlockM * 128;    // one 128-row x 64-element box
   static constexpr int kTileBytes = kChunks * kChunkBytes;
-  static constexpr int kStages = (D == 64) ? 4 : 3;    // K/V ring depth
+  static constexpr int kStages = (D == 64) ? 6 : 2;    // K/V ring depth
   static constexpr int kQ = 0;
-  static constexpr int kK = kQ + kTileBytes;
+  static constexpr int kK = kQ + kTilesPerCta * kTileBytes;
   static constexpr int kV = kK + kStages * kTileBytes;
   static constexpr int kBar = kV + kStages * kTileBytes;
-  static constexpr int kBarBytes = 256;
+  static constexpr int kBarBytes = 512;
   static constexpr int kTotal = kBar + kBarBytes + 1024;  // + slack for 1 KB alignment
 };
 
+constexpr int kMaxStages = 8;
 struct Barriers {
   uint64_t q_full;
-  uint64_t s_full[2];
-  uint64_t p_ready[2];
-  uint64_t pv_done;
+  uint64_t s_full[kTilesPerCta];
+  uint64_t p_ready[kTilesPerCta];
+  uint64_t o_done[kTilesPerCta];
   uint64_t fin;
-  uint64_t k_full[4];
-  uint64_t v_full[4];
-  uint64_t kv_empty[4];
+  uint64_t k_full[kMaxStages];
+  uint64_t v_full[kMaxStages];
+  uint64_t k_empty[kMaxStages];
+  uint64_t v_empty[kMaxStages];
   uint32_t tmem_base;
   uint32_t abort_flag;
 };
-static_assert(sizeof(Barriers) <= 256, "barrier block too large");
+static_assert(sizeof(Barriers) <= 512, "barrier block too large");
 static_assert(Layout<128>::kTotal <= 227 * 1024, "shared memory over the per-CTA limit");
 static_assert(Layout<64>::kTotal <= 227 * 1024, "shared memory over the per-CTA limit");
+static_assert(Layout<64>::kStages <= kMaxStages && Layout<128>::kStages <= kMaxStages, "ring");
 
 // Bounded wait on one barrier phase.  Returns false when the wait gave up:
 // either another role already raised the CTA abort flag (honour_abort), or
@@ -121,11 +139,11 @@ __device__ __forceinline__ bool warp_wait_phase(uint64_t* bar, uint32_t parity, 
 __device__ __forceinline__ void tma_tile(void* dst, const CUtensorMap* map, uint64_t* bar,
                                          int d0, int row, int head, int batch,
                                          const int (&pos)[3]) {
-  int c[4] = {d0, 0, 0, 0};
-  c[pos[0]] = row;
-  c[pos[1]] = head;
-  c[pos[2]] = batch;
-  tma_load_4d(dst, map, bar, c[0], c[1], c[2], c[3]);
+  // pos[] holds the map slot (1..3) of L, H and B; place the coordinates.
+  const int c1 = (pos[0] == 1) ? row : (pos[1] == 1) ? head : batch;
+  const int c2 = (pos[0] == 2) ? row : (pos[1] == 2) ? head : batch;
+  const int c3 = (pos[0] == 3) ? row : (pos[1] == 3) ? head : batch;
+  tma_load_4d(dst, map, bar, d0, c1, c2, c3);
 }
 
 template <bool BF16>
@@ -137,6 +155,222 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     __half2 v = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&v);
   }
+}
+
+// Work decomposition shared by every role of a CTA.
+struct Work {
+  int batch, head;
+  int tile[kTilesPerCta];  // query tile index of A and B
+  int n_kv[kTilesPerCta];  // key tiles each query tile visits (0: tile absent)
+  int n_kv_max;
+};
+
+template <int MODE>
+__device__ __forceinline__ Work make_work(const sdpa_impl::FwdParams& p) {
+  Work w;
+  const int pairs = (p.n_tiles + 1) >> 1;
+  const int bh = static_cast<int>(blockIdx.x / static_cast<unsigned>(pairs));
+  const int pr = pairs - 1 - static_cast<int>(blockIdx.x - bh * pairs);  // heaviest first
+  w.batch = bh / p.H;
+  w.head = bh - w.batch * p.H;
+  w.n_kv_max = 0;
+#pragma unroll
+  for (int t = 0; t < kTilesPerCta; ++t) {
+    const int qt = 2 * pr + t;
+    w.tile[t] = qt;
+    w.n_kv[t] = (qt >= p.n_tiles) ? 0 : ((MODE == sdpa_impl::kMaskCausal) ? qt + 1 : p.n_tiles);
+    w.n_kv_max = max(w.n_kv_max, w.n_kv[t]);
+  }
+  return w;
+}
+
+// ------------------------------------------------------------ softmax role
+// One warpgroup, one query tile: thread r of the group owns row r (TMEM lane r).
+// Both warpgroups run this one code path (t picks the tile at run time), so
+// the warps sharing an SM sub-partition also share instruction-cache lines.
+template <int D, int MODE, bool BF16>
+__device__ __forceinline__ void softmax_role(const sdpa_impl::FwdParams& p, const Work& w, int t,
+                                             Barriers* bars, uint32_t tmem, int wq, int lane) {
+  const int n = t ? w.n_kv[1] : w.n_kv[0];
+  if (n == 0) return;
+  const uint64_t limit = p.wait_limit_ns;
+  const int qt = t ? w.tile[1] : w.tile[0];
+  const uint32_t tS_base = tmem + (t ? 128u : 0u);
+  const uint32_t tO_base = tmem + 256u + (t ? static_cast<uint32_t>(D) : 0u);
+  const int r = wq * 32 + lane;
+  const int row_g = qt * kBlockM + r;
+  const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+  const uint32_t tS = tS_base + lane_off;
+  const uint32_t tO = tO_base + lane_off;
+  const float sl2 = p.scale_log2;
+  const bool pos_scale = sl2 >= 0.0f;
+  const float mval = pos_scale ? -INFINITY : INFINITY;  // a removed raw score
+  float m_used = -INFINITY;  // running max actually used in the exponentials
+  float l = 0.0f;            // running row sum of probabilities
+  bool ok = true;
+
+  for (int j = 0; j < n; ++j) {
+    if (!warp_wait_phase(&bars->s_full[t], j & 1, bars, limit, kSiteSFull)) {
+      ok = false;
+      break;
+    }
+    tc_fence_after();
+    float s[kBlockN];
+    {
+      uint32_t su[kBlockN];
+#pragma unroll
+      for (int c = 0; c < kBlockN / 32; ++c) tmem_ld32(tS + c * 32, su + c * 32);
+      tmem_ld_wait();
+#pragma unroll
+      for (int c = 0; c < kBlockN; ++c) s[c] = __uint_as_float(su[c]);
+    }
+    const int col0 = j * kBlockN;
+    const bool tail = col0 + kBlockN > p.L;
+    const bool masked_tile = (MODE == sdpa_impl::kMaskExplicit) || tail ||
+                             (MODE == sdpa_impl::kMaskCausal && j == qt);
+    if (masked_tile) {
+      if constexpr (MODE == sdpa_impl::kMaskExplicit) {
+        const bool row_ok = row_g < p.L;
+        const uint8_t* mrow = p.mask + static_cast<int64_t>(row_ok ? row_g : 0) * p.L + col0;
+        const bool vec = p.mask_vec16 && !tail && row_ok;
+#pragma unroll
+        for (int v = 0; v < kBlockN / 16; ++v) {
+          uint32_t mw[4];
+          if (vec) {
+            const uint4 x = __ldg(reinterpret_cast<const uint4*>(mrow) + v);
+            mw[0] = x.x;
+            mw[1] = x.y;
+            mw[2] = x.z;
+            mw[3] = x.w;
+          } else {
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+              uint32_t word = 0;
+#pragma unroll
+              for (int b = 0; b < 4; ++b) {
+                const int c = 16 * v + 4 * q4 + b;
+                const uint32_t byte = (row_ok && col0 + c < p.L) ? __ldg(mrow + c) : 1u;
+                word |= (byte != 0 ? 1u : 0u) << (8 * b);
+              }
+              mw[q4] = word;
+            }
+          }
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int c = 16 * v + e;
+            const bool removed =
+                (col0 + c >= p.L) || (((mw[e >> 2] >> (8 * (e & 3))) & 0xffu) != 0u);
+            s[c] = removed ? mval : s[c];
+          }
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < kBlockN; ++c) {
+          const bool removed =
+              (col0 + c >= p.L) || (MODE == sdpa_impl::kMaskCausal && col0 + c > row_g);
+          s[c] = removed ? mval : s[c];
+        }
+      }
+    }
+
+    // Row extremum of the raw scores (max for a positive scale): 8-way tree.
+    float e8[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) e8[i] = s[i];
+    if (pos_scale) {
+#pragma unroll
+      for (int c = 8; c < kBlockN; ++c) e8[c & 7] = fmaxf(e8[c & 7], s[c]);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) e8[i] = fmaxf(e8[i], e8[i + 4]);
+      e8[0] = fmaxf(fmaxf(e8[0], e8[1]), fmaxf(e8[2], e8[3]));
+    } else {
+#pragma unroll
+      for (int c = 8; c < kBlockN; ++c) e8[c & 7] = fminf(e8[c & 7], s[c]);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) e8[i] = fminf(e8[i], e8[i + 4]);
+      e8[0] = fminf(fminf(e8[0], e8[1]), fminf(e8[2], e8[3]));
+    }
+    const float ext = e8[0];
+    const float m_tile = (ext == mval) ? -INFINITY : ext * sl2;
+    const bool need = m_tile > m_used + kRescaleLog2;
+    float alpha = 1.0f;
+    if (need) {
+      alpha = ex2(m_used - m_tile);  // 0 when nothing was admitted before
+      m_used = m_tile;
+      l *= alpha;
+    }
+    const float neg_m = (m_used == -INFINITY) ? 0.0f : -m_used;
+
+    uint32_t pk[kBlockN / 2];
+    float rs8[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) rs8[i] = 0.0f;
+#pragma unroll
+    for (int c = 0; c < kBlockN / 2; ++c) {
+      // A removed score is +-inf with the sign that makes s * sl2 = -inf, so
+      // its probability is exactly 0 (sl2 is never 0: the host maps a zero
+      // scale to +-FLT_MIN, which gives the same all-ones weights).
+      const float p0 = ex2(fmaf(s[2 * c], sl2, neg_m));
+      const float p1 = ex2(fmaf(s[2 * c + 1], sl2, neg_m));
+      rs8[c & 7] += p0 + p1;
+      pk[c] = pack2<BF16>(p0, p1);
+    }
+    // P_j overwrites the first 64 columns of this tile's score buffer.
+    tmem_st32(tS + 0, pk);
+    tmem_st32(tS + 32, pk + 32);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) rs8[i] += rs8[i + 4];
+    l += (rs8[0] + rs8[1]) + (rs8[2] + rs8[3]);
+
+    if (j > 0) {
+      // Consume PV_{j-1}'s completion in order (keeps phase parity exact);
+      // it is needed anyway before O may be rescaled.
+      if (!warp_wait_phase(&bars->o_done[t], (j - 1) & 1, bars, limit, kSiteODone)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      if (__any_sync(0xffffffffu, need)) {
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tO + c * 32, o);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+          tmem_st32(tO + c * 32, o);
+        }
+      }
+    }
+    tmem_st_wait();
+    tc_fence_before();
+    mbar_arrive(&bars->p_ready[t]);
+  }
+
+  if (ok && warp_wait_phase(&bars->o_done[t], (n - 1) & 1, bars, limit, kSiteODone)) {
+    tc_fence_after();
+    const float inv_l = (l > 0.0f) ? (1.0f / l) : 0.0f;
+    uint16_t* orow = reinterpret_cast<uint16_t*>(p.out) + w.batch * p.o_sb + w.head * p.o_sh +
+                     static_cast<int64_t>(row_g) * p.o_sl;
+#pragma unroll
+    for (int c = 0; c < D / 32; ++c) {
+      uint32_t o[32];
+      tmem_ld32(tO + c * 32, o);
+      tmem_ld_wait();
+      uint32_t pw[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e)
+        pw[e] = pack2<BF16>(__uint_as_float(o[2 * e]) * inv_l,
+                            __uint_as_float(o[2 * e + 1]) * inv_l);
+      if (row_g < p.L) {
+        uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+        for (int v = 0; v < 4; ++v)
+          dst[v] = make_uint4(pw[4 * v], pw[4 * v + 1], pw[4 * v + 2], pw[4 * v + 3]);
+      }
+    }
+  }
+  tc_fence_before();
 }
 
 // ------------------------------------------------------------------ kernel
@@ -154,28 +388,24 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  // Launch order walks one head's query tiles (heaviest first) before the
-  // next head, so the CTAs resident at any time share a few heads' K/V in L2.
-  const int bh = static_cast<int>(blockIdx.x / static_cast<unsigned>(p.n_tiles));
-  const int batch = bh / p.H;
-  const int head = bh - batch * p.H;
-  const int q_tile = p.n_tiles - 1 - static_cast<int>(blockIdx.x - bh * p.n_tiles);
-  const int n_kv = (MODE == sdpa_impl::kMaskCausal) ? (q_tile + 1) : p.n_tiles;
+  const Work w = make_work<MODE>(p);
   const uint64_t limit = p.wait_limit_ns;
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
-    mbar_init(&bars->s_full[0], 1);
-    mbar_init(&bars->s_full[1], 1);
-    mbar_init(&bars->p_ready[0], kBlockM);
-    mbar_init(&bars->p_ready[1], kBlockM);
-    mbar_init(&bars->pv_done, 1);
+#pragma unroll
+    for (int t = 0; t < kTilesPerCta; ++t) {
+      mbar_init(&bars->s_full[t], 1);
+      mbar_init(&bars->p_ready[t], kBlockM);
+      mbar_init(&bars->o_done[t], 1);
+    }
     mbar_init(&bars->fin, 1);
 #pragma unroll
     for (int s = 0; s < Lay::kStages; ++s) {
       mbar_init(&bars->k_full[s], 1);
       mbar_init(&bars->v_full[s], 1);
-      mbar_init(&bars->kv_empty[s], 1);
+      mbar_init(&bars->k_empty[s], 1);
+      mbar_init(&bars->v_empty[s], 1);
     }
     bars->abort_flag = 0;
     fence_barrier_init();
@@ -193,49 +423,62 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
-  const uint32_t tS0 = tmem;        // score / probability buffer 0: columns [0, 128)
-  const uint32_t tS1 = tmem + 128;  // score / probability buffer 1: columns [128, 256)
-  const uint32_t tO = tmem + 256;   // output accumulator: columns [256, 256 + D)
+  // TMEM columns: S_A [0,128), S_B [128,256), O_A [256, 256+D), O_B [256+D, 256+2D)
+  const uint32_t tS[kTilesPerCta] = {tmem, tmem + 128};
+  const uint32_t tO[kTilesPerCta] = {tmem + 256, tmem + 256 + D};
 
+  if (warp >= 4) {
+    // ------------------------------------------- softmax / output warps
+    regs_increase<kRegsSoftmax>();
+    // warps 4..7 -> tile A, 8..11 -> tile B
+    softmax_role<D, MODE, BF16>(p, w, (warp - 4) >> 2, bars, tmem, warp & 3, lane);
+  } else {
+    regs_decrease<kRegsControl>();
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer
     if (lane == 0) {
-      int issued[4] = {0, 0, 0, 0};
+      // Key / value tiles issued so far (a give-up drains them below).
+      int k_end = 0, v_end = 0;
       if (!p.debug_withhold_q) {
-        mbar_arrive_expect_tx(&bars->q_full, Lay::kTileBytes);
+        const int nq = (w.n_kv[1] > 0) ? 2 : 1;
+        mbar_arrive_expect_tx(&bars->q_full, nq * Lay::kTileBytes);
+        for (int t = 0; t < nq; ++t)
 #pragma unroll
-        for (int c = 0; c < Lay::kChunks; ++c)
-          tma_tile(sQ + c * Lay::kChunkBytes, &p.tm_q, &bars->q_full, c * 64, q_tile * kBlockM,
-                   head, batch, p.pos_q);
+          for (int c = 0; c < Lay::kChunks; ++c)
+            tma_tile(sQ + t * Lay::kTileBytes + c * Lay::kChunkBytes, &p.tm_q, &bars->q_full,
+                     c * 64, w.tile[t] * kBlockM, w.head, w.batch, p.pos_q);
       }
-      for (int j = 0; j < n_kv; ++j) {
+      for (int j = 0; j < w.n_kv_max; ++j) {
         const int s = j % Lay::kStages;
         const int use = j / Lay::kStages;
-        if (use > 0 &&
-            !wait_phase(&bars->kv_empty[s], (use - 1) & 1, bars, limit, kSiteKvEmpty))
+        if (use > 0 && !wait_phase(&bars->k_empty[s], (use - 1) & 1, bars, limit, kSiteEmpty))
           break;
         mbar_arrive_expect_tx(&bars->k_full[s], Lay::kTileBytes);
 #pragma unroll
         for (int c = 0; c < Lay::kChunks; ++c)
           tma_tile(sK + s * Lay::kTileBytes + c * Lay::kChunkBytes, &p.tm_k, &bars->k_full[s],
-                   c * 64, j * kBlockN, head, batch, p.pos_k);
+                   c * 64, j * kBlockN, w.head, w.batch, p.pos_k);
+        k_end = j + 1;
+        if (use > 0 && !wait_phase(&bars->v_empty[s], (use - 1) & 1, bars, limit, kSiteEmpty))
+          break;
         mbar_arrive_expect_tx(&bars->v_full[s], Lay::kTileBytes);
 #pragma unroll
         for (int c = 0; c < Lay::kChunks; ++c)
           tma_tile(sV + s * Lay::kTileBytes + c * Lay::kChunkBytes, &p.tm_v, &bars->v_full[s],
-                   c * 64, j * kBlockN, head, batch, p.pos_v);
-        issued[s] = use + 1;
+                   c * 64, j * kBlockN, w.head, w.batch, p.pos_v);
+        v_end = j + 1;
       }
       // Drain: every load issued must have landed before shared memory is
       // released (only matters when a wait gave up).
-#pragma unroll
-      for (int s = 0; s < Lay::kStages; ++s)
-        if (issued[s] > 0) {
-          wait_phase(&bars->k_full[s], (issued[s] - 1) & 1, bars, limit, kSiteDrain, false);
-          wait_phase(&bars->v_full[s], (issued[s] - 1) & 1, bars, limit, kSiteDrain, false);
-        }
-      if (!p.debug_withhold_q)
-        wait_phase(&bars->q_full, 0, bars, limit, kSiteDrain, false);
+      // The last tile issued into stage s is the largest j < end with
+      // j % kStages == s; its use count is j / kStages.
+      for (int j = max(0, k_end - Lay::kStages); j < k_end; ++j)
+        wait_phase(&bars->k_full[j % Lay::kStages], (j / Lay::kStages) & 1, bars, limit,
+                   kSiteDrain, false);
+      for (int j = max(0, v_end - Lay::kStages); j < v_end; ++j)
+        wait_phase(&bars->v_full[j % Lay::kStages], (j / Lay::kStages) & 1, bars, limit,
+                   kSiteDrain, false);
+      if (!p.debug_withhold_q) wait_phase(&bars->q_full, 0, bars, limit, kSiteDrain, false);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------- MMA issuer
@@ -247,55 +490,76 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t aV = smem_addr(sV);
       bool issued_any = false;
 
-      // O += P_jp V_jp, with P_jp read from the TMEM score buffer it replaced.
-      auto issue_pv = [&](int jp) -> bool {
-        const int bp = jp & 1;
-        const int sp = jp % Lay::kStages;
-        if (!wait_phase(&bars->v_full[sp], (jp / Lay::kStages) & 1, bars, limit, kSiteKvFull))
-          return false;
-        if (!wait_phase(&bars->p_ready[bp], (jp >> 1) & 1, bars, limit, kSitePReady))
-          return false;
-        tc_fence_after();
-        const uint32_t tP = bp ? tS1 : tS0;
+      // S_t = Q_t K^T from key stage s.
+      auto issue_s = [&](int t, int s) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const int c = kk >> 2;           // which 64-wide chunk of D
+          const int koff = (kk & 3) * 32;  // 16 elements = 32 B inside the atom
+          const uint64_t adesc = smem_desc_sw128(
+              aQ + t * Lay::kTileBytes + c * Lay::kChunkBytes + koff, 16, 1024);
+          const uint64_t bdesc =
+              smem_desc_sw128(aK + s * Lay::kTileBytes + c * Lay::kChunkBytes + koff, 16, 1024);
+          mma_ss(tS[t], adesc, bdesc, idS, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&bars->s_full[t]);
+      };
+      // O_t (+)= P_t V from value stage s, P_t read from the first 64 columns of S_t.
+      auto issue_pv = [&](int t, int s, bool accumulate) {
 #pragma unroll
         for (int kk = 0; kk < kBlockN / 16; ++kk) {
-          // V tile, keys kk*16 .. +16: 16 rows of 128 B per 64-wide chunk,
-          // chunks 64 elements of D apart (LBO), 8-row groups 1 KB apart (SBO).
-          const uint64_t bdesc = smem_desc_sw128(
-              aV + sp * Lay::kTileBytes + kk * 16 * 128, Lay::kChunkBytes, 1024);
-          mma_ts(tO, tP + kk * 8, bdesc, idPV, (jp > 0 || kk > 0) ? 1u : 0u);
+          // V tile, keys kk*16 .. +16: rows of 128 B per 64-wide chunk of D,
+          // chunks one box apart (LBO), 8-row groups 1 KB apart (SBO).
+          const uint64_t bdesc = smem_desc_sw128(aV + s * Lay::kTileBytes + kk * 16 * 128,
+                                                 Lay::kChunkBytes, 1024);
+          mma_ts(tO[t], tS[t] + kk * 8, bdesc, idPV, (accumulate || kk > 0) ? 1u : 0u);
         }
-        mma_commit(&bars->pv_done);
-        mma_commit(&bars->kv_empty[sp]);
-        return true;
+        mma_commit(&bars->o_done[t]);
       };
 
-      bool ok = wait_phase(&bars->q_full, 0, bars, limit, kSiteQFull);
+      bool ok = wait_phase(&bars->q_full, 0, bars, limit, kSiteQFull) &&
+                wait_phase(&bars->k_full[0], 0, bars, limit, kSiteKFull);
       if (ok) {
         tc_fence_after();
-        for (int j = 0; j < n_kv && ok; ++j) {
+#pragma unroll
+        for (int t = 0; t < kTilesPerCta; ++t)
+          if (w.n_kv[t] > 0) issue_s(t, 0);
+        mma_commit(&bars->k_empty[0]);
+        issued_any = true;
+        for (int j = 0; j < w.n_kv_max && ok; ++j) {
           const int s = j % Lay::kStages;
-          if (!wait_phase(&bars->k_full[s], (j / Lay::kStages) & 1, bars, limit,
-                          kSiteKvFull)) {
+          const int s1 = (j + 1) % Lay::kStages;
+          if (!wait_phase(&bars->v_full[s], (j / Lay::kStages) & 1, bars, limit, kSiteVFull)) {
             ok = false;
             break;
           }
-          tc_fence_after();
-          const uint32_t tS = (j & 1) ? tS1 : tS0;
+          bool k_next = false;
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const int c = kk >> 2;              // which 64-wide chunk of D
-            const int koff = (kk & 3) * 32;     // 16 elements = 32 B inside the atom
-            const uint64_t adesc = smem_desc_sw128(aQ + c * Lay::kChunkBytes + koff, 16, 1024);
-            const uint64_t bdesc = smem_desc_sw128(
-                aK + s * Lay::kTileBytes + c * Lay::kChunkBytes + koff, 16, 1024);
-            mma_ss(tS, adesc, bdesc, idS, kk > 0 ? 1u : 0u);
+          for (int t = 0; t < kTilesPerCta; ++t) {
+            if (j >= w.n_kv[t]) continue;
+            if (!wait_phase(&bars->p_ready[t], j & 1, bars, limit, kSitePReady)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_pv(t, s, j > 0);
+            if (j + 1 < w.n_kv[t]) {
+              if (!k_next) {
+                if (!wait_phase(&bars->k_full[s1], ((j + 1) / Lay::kStages) & 1, bars, limit,
+                                kSiteKFull)) {
+                  ok = false;
+                  break;
+                }
+                tc_fence_after();
+                k_next = true;
+              }
+              issue_s(t, s1);
+            }
           }
-          mma_commit(&bars->s_full[j & 1]);
-          issued_any = true;
-          if (j > 0 && !issue_pv(j - 1)) ok = false;
+          if (!ok) break;
+          mma_commit(&bars->v_empty[s]);
+          if (k_next) mma_commit(&bars->k_empty[s1]);
         }
-        if (ok && n_kv > 0) ok = issue_pv(n_kv - 1);
       }
       if (issued_any) {
         // Everything issued must finish before TMEM is released.
@@ -303,176 +567,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         wait_phase(&bars->fin, 0, bars, limit, kSiteDrain, false);
       }
     }
-  } else if (warp >= 4) {
-    // ------------------------------------------- softmax / output warps
-    const int wq = warp & 3;
-    const int r = wq * 32 + lane;            // row in tile == TMEM lane
-    const int row_g = q_tile * kBlockM + r;  // query index in [0, L) when valid
-    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
-    const float sl2 = p.scale_log2;
-    const bool pos_scale = sl2 >= 0.0f;
-    const float mval = pos_scale ? -INFINITY : INFINITY;  // a removed raw score
-    float m_used = -INFINITY;  // running max actually used in the exponentials
-    float l = 0.0f;            // running row sum of probabilities
-    bool ok = true;
-
-    for (int j = 0; j < n_kv; ++j) {
-      const int b = j & 1;
-      const uint32_t tS = (b ? tS1 : tS0) + lane_off;
-      if (!warp_wait_phase(&bars->s_full[b], (j >> 1) & 1, bars, limit, kSiteSFull)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      float s[kBlockN];
-      {
-        uint32_t su[kBlockN];
-#pragma unroll
-        for (int c = 0; c < kBlockN / 32; ++c) tmem_ld32(tS + c * 32, su + c * 32);
-        tmem_ld_wait();
-#pragma unroll
-        for (int c = 0; c < kBlockN; ++c) s[c] = __uint_as_float(su[c]);
-      }
-      const int col0 = j * kBlockN;
-      const bool tail = col0 + kBlockN > p.L;
-      const bool masked_tile = (MODE == sdpa_impl::kMaskExplicit) || tail ||
-                               (MODE == sdpa_impl::kMaskCausal && j == q_tile);
-      if (masked_tile) {
-        if constexpr (MODE == sdpa_impl::kMaskExplicit) {
-          uint32_t mw[kBlockN / 4];
-          if (row_g < p.L) {
-            const uint8_t* mrow = p.mask + static_cast<int64_t>(row_g) * p.L + col0;
-            if (p.mask_vec16 && !tail) {
-#pragma unroll
-              for (int v = 0; v < kBlockN / 16; ++v) {
-                const uint4 x = __ldg(reinterpret_cast<const uint4*>(mrow) + v);
-                mw[4 * v + 0] = x.x;
-                mw[4 * v + 1] = x.y;
-                mw[4 * v + 2] = x.z;
-                mw[4 * v + 3] = x.w;
-              }
-            } else {
-#pragma unroll
-              for (int w = 0; w < kBlockN / 4; ++w) {
-                uint32_t word = 0;
-#pragma unroll
-                for (int t = 0; t < 4; ++t) {
-                  const int c = 4 * w + t;
-                  const uint32_t byte = (col0 + c < p.L) ? __ldg(mrow + c) : 1u;
-                  word |= (byte != 0 ? 1u : 0u) << (8 * t);
-                }
-                mw[w] = word;
-              }
-            }
-          } else {
-#pragma unroll
-            for (int w = 0; w < kBlockN / 4; ++w) mw[w] = 0x01010101u;
-          }
-#pragma unroll
-          for (int c = 0; c < kBlockN; ++c) {
-            const bool removed =
-                (col0 + c >= p.L) || (((mw[c >> 2] >> (8 * (c & 3))) & 0xffu) != 0u);
-            s[c] = removed ? mval : s[c];
-          }
-        } else {
-#pragma unroll
-          for (int c = 0; c < kBlockN; ++c) {
-            const bool removed = (col0 + c >= p.L) ||
-                                 (MODE == sdpa_impl::kMaskCausal && col0 + c > row_g);
-            s[c] = removed ? mval : s[c];
-          }
-        }
-      }
-
-      // Row extremum of the raw scores (max for a positive scale).
-      float ext = s[0];
-      if (pos_scale) {
-#pragma unroll
-        for (int c = 1; c < kBlockN; ++c) ext = fmaxf(ext, s[c]);
-      } else {
-#pragma unroll
-        for (int c = 1; c < kBlockN; ++c) ext = fminf(ext, s[c]);
-      }
-      const float m_tile = (ext == mval) ? -INFINITY : ext * sl2;
-      const bool need = m_tile > m_used + kRescaleLog2;
-      float alpha = 1.0f;
-      if (need) {
-        alpha = ex2(m_used - m_tile);  // 0 when nothing was admitted before
-        m_used = m_tile;
-        l *= alpha;
-      }
-      const float neg_m = (m_used == -INFINITY) ? 0.0f : -m_used;
-
-      uint32_t pk[kBlockN / 2];
-      float rs = 0.0f;
-#pragma unroll
-      for (int c = 0; c < kBlockN / 2; ++c) {
-        float p0 = ex2(fmaf(s[2 * c], sl2, neg_m));
-        float p1 = ex2(fmaf(s[2 * c + 1], sl2, neg_m));
-        if (masked_tile) {
-          p0 = (s[2 * c] == mval) ? 0.0f : p0;
-          p1 = (s[2 * c + 1] == mval) ? 0.0f : p1;
-        }
-        rs += p0 + p1;
-        pk[c] = pack2<BF16>(p0, p1);
-      }
-      l += rs;
-      // P_j overwrites the first 64 columns of its own score buffer.
-      tmem_st32(tS + 0, pk);
-      tmem_st32(tS + 32, pk + 32);
-
-      if (j > 0) {
-        // Consume PV_{j-1}'s completion in order (keeps phase parity exact);
-        // it is needed anyway before O may be rescaled.
-        if (!warp_wait_phase(&bars->pv_done, (j - 1) & 1, bars, limit, kSitePvDone)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        if (__any_sync(0xffffffffu, need)) {
-#pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t o[32];
-            tmem_ld32(tO + lane_off + c * 32, o);
-            tmem_ld_wait();
-#pragma unroll
-            for (int t = 0; t < 32; ++t) o[t] = __float_as_uint(__uint_as_float(o[t]) * alpha);
-            tmem_st32(tO + lane_off + c * 32, o);
-          }
-        }
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(&bars->p_ready[b]);
-    }
-
-    if (ok && n_kv > 0 &&
-        warp_wait_phase(&bars->pv_done, (n_kv - 1) & 1, bars, limit, kSitePvDone)) {
-      tc_fence_after();
-      const float inv_l = (l > 0.0f) ? (1.0f / l) : 0.0f;
-      using elem_t = uint16_t;
-      elem_t* orow = reinterpret_cast<elem_t*>(p.out) + batch * p.o_sb + head * p.o_sh +
-                     static_cast<int64_t>(row_g) * p.o_sl;
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t o[32];
-        tmem_ld32(tO + lane_off + c * 32, o);
-        tmem_ld_wait();
-        uint32_t w[16];
-#pragma unroll
-        for (int t = 0; t < 16; ++t)
-          w[t] = pack2<BF16>(__uint_as_float(o[2 * t]) * inv_l,
-                             __uint_as_float(o[2 * t + 1]) * inv_l);
-        if (row_g < p.L) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
-#pragma unroll
-          for (int v = 0; v < 4; ++v)
-            dst[v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
-        }
-      }
-    }
-    tc_fence_before();
   }
+  }  // control warpgroup
 
   __syncthreads();
   if (warp == 1) {
@@ -488,12 +584,19 @@ cudaError_t launch_one(const sdpa_impl::FwdParams& p, cudaStream_t stream) {
   constexpr int smem = Layout<D>::kTotal;
   static bool configured = false;  // one attribute call per instantiation
   if (!configured) {
-    cudaError_t e =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    // The in-kernel register split assumes the launch reserves kLaunchRegs
+    // per thread; never launch a build where that does not hold (the
+    // softmax warpgroups would wait forever for registers).
+    cudaFuncAttributes attr{};
+    cudaError_t e = cudaFuncGetAttributes(&attr, kern);
+    if (e != cudaSuccess) return e;
+    if (attr.numRegs != static_cast<int>(kLaunchRegs)) return cudaErrorInvalidConfiguration;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  dim3 grid(static_cast<unsigned>(p.n_tiles) * static_cast<unsigned>(p.B * p.H));
+  const unsigned pairs = static_cast<unsigned>((p.n_tiles + 1) / 2);
+  dim3 grid(pairs * static_cast<unsigned>(p.B * p.H));
   kern<<<grid, kThreads, smem, stream>>>(p);
   return cudaGetLastError();
 }

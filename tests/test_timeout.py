@@ -1,0 +1,39 @@
+"""Failure detection without a GPU fault: every barrier wait in the kernel is
+bounded in time.  The test hook withholds the query-tile load, so the MMA and
+softmax roles wait on a phase that never completes; each wait gives up after
+the (shortened) limit, the CTA drains what it issued, frees its tensor memory
+and records a status bit.  The host then reads SDPA_ERR_DEVICE_TIMEOUT and the
+context stays usable: the next normal call is correct."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import sdpa_inputs
+
+pytestmark = pytest.mark.gpu
+
+
+def test_withheld_load_times_out_and_recovers(sdpa_lib):
+    q, k, v = sdpa_inputs.custom((1, 1, 256, 128), seed=21)
+    qd, kd, vd = (x.cuda() for x in (q, k, v))
+    assert sdpa_lib.sdpa_last_device_status()[0] == 0
+    try:
+        sdpa_lib.sdpa_debug_set_wait_limit_ns(50_000_000)  # 50 ms per wait
+        sdpa_lib.sdpa_debug_withhold_q_load(True)
+        sdpa_lib.sdpa_forward(qd, kd, vd, is_causal=True)
+        rc, detail = sdpa_lib.sdpa_last_device_status()
+    finally:
+        sdpa_lib.sdpa_debug_withhold_q_load(False)
+        sdpa_lib.sdpa_debug_set_wait_limit_ns(0)
+    assert rc == 8, f"expected SDPA_ERR_DEVICE_TIMEOUT, got {rc}"
+    assert detail & 1
+    assert detail & ((1 << 1) | (1 << 4)), f"expected a Q or S wait site, bits {detail:#x}"
+    # the status word was cleared and the context still works
+    assert sdpa_lib.sdpa_last_device_status()[0] == 0
+    out = sdpa_lib.sdpa_forward(qd, kd, vd, is_causal=True)
+    assert sdpa_lib.sdpa_last_device_status()[0] == 0
+    ref = oracle.sdpa(q, k, v, is_causal=True)
+    got = out.double().cpu().numpy()
+    assert np.linalg.norm(got - ref) / np.linalg.norm(ref) <= 1e-2
+    assert torch.cuda.synchronize() is None
