@@ -273,22 +273,29 @@ __device__ __forceinline__ void softmax_role(const sdpa_impl::FwdParams& p, cons
       }
     }
 
-    // Row extremum of the raw scores (max for a positive scale): 8-way tree.
+    // Row extremum of the raw scores (max for a positive scale): eight
+    // independent chains of three-input max, then a short tree.
     float e8[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) e8[i] = s[i];
     if (pos_scale) {
 #pragma unroll
-      for (int c = 8; c < kBlockN; ++c) e8[c & 7] = fmaxf(e8[c & 7], s[c]);
+      for (int c = 8; c < kBlockN; c += 16)
 #pragma unroll
-      for (int i = 0; i < 4; ++i) e8[i] = fmaxf(e8[i], e8[i + 4]);
-      e8[0] = fmaxf(fmaxf(e8[0], e8[1]), fmaxf(e8[2], e8[3]));
+        for (int i = 0; i < 8; ++i) e8[i] = max3f(e8[i], s[c + i], s[c + 8 + i < kBlockN ? c + 8 + i : c + i]);
+      e8[0] = max3f(e8[0], e8[1], e8[2]);
+      e8[3] = max3f(e8[3], e8[4], e8[5]);
+      e8[6] = fmaxf(e8[6], e8[7]);
+      e8[0] = max3f(e8[0], e8[3], e8[6]);
     } else {
 #pragma unroll
-      for (int c = 8; c < kBlockN; ++c) e8[c & 7] = fminf(e8[c & 7], s[c]);
+      for (int c = 8; c < kBlockN; c += 16)
 #pragma unroll
-      for (int i = 0; i < 4; ++i) e8[i] = fminf(e8[i], e8[i + 4]);
-      e8[0] = fminf(fminf(e8[0], e8[1]), fminf(e8[2], e8[3]));
+        for (int i = 0; i < 8; ++i) e8[i] = min3f(e8[i], s[c + i], s[c + 8 + i < kBlockN ? c + 8 + i : c + i]);
+      e8[0] = min3f(e8[0], e8[1], e8[2]);
+      e8[3] = min3f(e8[3], e8[4], e8[5]);
+      e8[6] = fminf(e8[6], e8[7]);
+      e8[0] = min3f(e8[0], e8[3], e8[6]);
     }
     const float ext = e8[0];
     const float m_tile = (ext == mval) ? -INFINITY : ext * sl2;
@@ -302,25 +309,28 @@ __device__ __forceinline__ void softmax_role(const sdpa_impl::FwdParams& p, cons
     const float neg_m = (m_used == -INFINITY) ? 0.0f : -m_used;
 
     uint32_t pk[kBlockN / 2];
-    float rs8[8];
+    float rs[8];  // four packed pairs of partial row sums
 #pragma unroll
-    for (int i = 0; i < 8; ++i) rs8[i] = 0.0f;
+    for (int i = 0; i < 8; ++i) rs[i] = 0.0f;
 #pragma unroll
     for (int c = 0; c < kBlockN / 2; ++c) {
       // A removed score is +-inf with the sign that makes s * sl2 = -inf, so
       // its probability is exactly 0 (sl2 is never 0: the host maps a zero
       // scale to +-FLT_MIN, which gives the same all-ones weights).
-      const float p0 = ex2(fmaf(s[2 * c], sl2, neg_m));
-      const float p1 = ex2(fmaf(s[2 * c + 1], sl2, neg_m));
-      rs8[c & 7] += p0 + p1;
+      float x0, x1;
+      fma2_bcast(x0, x1, s[2 * c], s[2 * c + 1], sl2, neg_m);
+      const float p0 = ex2(x0);
+      const float p1 = ex2(x1);
+      add2_acc(rs[2 * (c & 3)], rs[2 * (c & 3) + 1], p0, p1);
       pk[c] = pack2<BF16>(p0, p1);
     }
     // P_j overwrites the first 64 columns of this tile's score buffer.
     tmem_st32(tS + 0, pk);
     tmem_st32(tS + 32, pk + 32);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) rs8[i] += rs8[i + 4];
-    l += (rs8[0] + rs8[1]) + (rs8[2] + rs8[3]);
+    add2_acc(rs[0], rs[1], rs[2], rs[3]);
+    add2_acc(rs[4], rs[5], rs[6], rs[7]);
+    add2_acc(rs[0], rs[1], rs[4], rs[5]);
+    l += rs[0] + rs[1];
 
     if (j > 0) {
       // Consume PV_{j-1}'s completion in order (keeps phase parity exact);
@@ -336,8 +346,9 @@ __device__ __forceinline__ void softmax_role(const sdpa_impl::FwdParams& p, cons
           uint32_t o[32];
           tmem_ld32(tO + c * 32, o);
           tmem_ld_wait();
+          float* of = reinterpret_cast<float*>(o);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+          for (int e = 0; e < 32; e += 2) mul2_bcast(of[e], of[e + 1], alpha);
           tmem_st32(tO + c * 32, o);
         }
       }
@@ -434,138 +445,150 @@ __global__ void __launch_bounds__(kThreads, 1)
     softmax_role<D, MODE, BF16>(p, w, (warp - 4) >> 2, bars, tmem, warp & 3, lane);
   } else {
     regs_decrease<kRegsControl>();
+  // Both control warps run their loops with all 32 lanes, so loop variables
+  // and descriptors stay warp-uniform; one elected lane issues each TMA copy,
+  // MMA and commit.  (Issuing from a lane-0-only branch costs about 2.5x more
+  // per tcgen05.mma and starves the tensor core.)
+  const bool leader = elect_one();
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      // Key / value tiles issued so far (a give-up drains them below).
-      int k_end = 0, v_end = 0;
-      if (!p.debug_withhold_q) {
-        const int nq = (w.n_kv[1] > 0) ? 2 : 1;
-        mbar_arrive_expect_tx(&bars->q_full, nq * Lay::kTileBytes);
-        for (int t = 0; t < nq; ++t)
+    // Key / value tiles issued so far (a give-up drains them below).
+    int k_end = 0, v_end = 0;
+    if (!p.debug_withhold_q && leader) {
+      const int nq = (w.n_kv[1] > 0) ? 2 : 1;
+      mbar_arrive_expect_tx(&bars->q_full, nq * Lay::kTileBytes);
+      for (int t = 0; t < nq; ++t)
 #pragma unroll
-          for (int c = 0; c < Lay::kChunks; ++c)
-            tma_tile(sQ + t * Lay::kTileBytes + c * Lay::kChunkBytes, &p.tm_q, &bars->q_full,
-                     c * 64, w.tile[t] * kBlockM, w.head, w.batch, p.pos_q);
-      }
-      for (int j = 0; j < w.n_kv_max; ++j) {
-        const int s = j % Lay::kStages;
-        const int use = j / Lay::kStages;
-        if (use > 0 && !wait_phase(&bars->k_empty[s], (use - 1) & 1, bars, limit, kSiteEmpty))
-          break;
+        for (int c = 0; c < Lay::kChunks; ++c)
+          tma_tile(sQ + t * Lay::kTileBytes + c * Lay::kChunkBytes, &p.tm_q, &bars->q_full,
+                   c * 64, w.tile[t] * kBlockM, w.head, w.batch, p.pos_q);
+    }
+    for (int j = 0; j < w.n_kv_max; ++j) {
+      const int s = j % Lay::kStages;
+      const int use = j / Lay::kStages;
+      if (use > 0 &&
+          !warp_wait_phase(&bars->k_empty[s], (use - 1) & 1, bars, limit, kSiteEmpty))
+        break;
+      if (leader) {
         mbar_arrive_expect_tx(&bars->k_full[s], Lay::kTileBytes);
 #pragma unroll
         for (int c = 0; c < Lay::kChunks; ++c)
           tma_tile(sK + s * Lay::kTileBytes + c * Lay::kChunkBytes, &p.tm_k, &bars->k_full[s],
                    c * 64, j * kBlockN, w.head, w.batch, p.pos_k);
-        k_end = j + 1;
-        if (use > 0 && !wait_phase(&bars->v_empty[s], (use - 1) & 1, bars, limit, kSiteEmpty))
-          break;
+      }
+      k_end = j + 1;
+      if (use > 0 &&
+          !warp_wait_phase(&bars->v_empty[s], (use - 1) & 1, bars, limit, kSiteEmpty))
+        break;
+      if (leader) {
         mbar_arrive_expect_tx(&bars->v_full[s], Lay::kTileBytes);
 #pragma unroll
         for (int c = 0; c < Lay::kChunks; ++c)
           tma_tile(sV + s * Lay::kTileBytes + c * Lay::kChunkBytes, &p.tm_v, &bars->v_full[s],
                    c * 64, j * kBlockN, w.head, w.batch, p.pos_v);
-        v_end = j + 1;
       }
-      // Drain: every load issued must have landed before shared memory is
-      // released (only matters when a wait gave up).
-      // The last tile issued into stage s is the largest j < end with
-      // j % kStages == s; its use count is j / kStages.
-      for (int j = max(0, k_end - Lay::kStages); j < k_end; ++j)
-        wait_phase(&bars->k_full[j % Lay::kStages], (j / Lay::kStages) & 1, bars, limit,
-                   kSiteDrain, false);
-      for (int j = max(0, v_end - Lay::kStages); j < v_end; ++j)
-        wait_phase(&bars->v_full[j % Lay::kStages], (j / Lay::kStages) & 1, bars, limit,
-                   kSiteDrain, false);
-      if (!p.debug_withhold_q) wait_phase(&bars->q_full, 0, bars, limit, kSiteDrain, false);
+      v_end = j + 1;
     }
+    // Drain: every load issued must have landed before shared memory is
+    // released (only matters when a wait gave up).  The last tile issued into
+    // a stage is the largest j < end with that j % kStages.
+    for (int j = max(0, k_end - Lay::kStages); j < k_end; ++j)
+      wait_phase(&bars->k_full[j % Lay::kStages], (j / Lay::kStages) & 1, bars, limit,
+                 kSiteDrain, false);
+    for (int j = max(0, v_end - Lay::kStages); j < v_end; ++j)
+      wait_phase(&bars->v_full[j % Lay::kStages], (j / Lay::kStages) & 1, bars, limit,
+                 kSiteDrain, false);
+    if (!p.debug_withhold_q) wait_phase(&bars->q_full, 0, bars, limit, kSiteDrain, false);
   } else if (warp == 1) {
     // ------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idS = idesc_f16_f32acc(BF16, false, kBlockM, kBlockN);
-      constexpr uint32_t idPV = idesc_f16_f32acc(BF16, true, kBlockM, D);
-      const uint32_t aQ = smem_addr(sQ);
-      const uint32_t aK = smem_addr(sK);
-      const uint32_t aV = smem_addr(sV);
-      bool issued_any = false;
+    constexpr uint32_t idS = idesc_f16_f32acc(BF16, false, kBlockM, kBlockN);
+    constexpr uint32_t idPV = idesc_f16_f32acc(BF16, true, kBlockM, D);
+    // Descriptor low words of the Q, K and V bases; every operand of every
+    // MMA below is one of these plus a compile-time or per-stage offset.
+    constexpr uint32_t kHiKMajor = desc_hi_sw128(1024);  // 8-row groups 1 KB apart
+    constexpr uint32_t kHiV = desc_hi_sw128(1024);
+    const uint32_t q_lo = desc_lo_sw128(smem_addr(sQ), 16);
+    const uint32_t k_lo = desc_lo_sw128(smem_addr(sK), 16);
+    // V is MN-major: its 64-wide chunks of D are one box apart (LBO).
+    const uint32_t v_lo = desc_lo_sw128(smem_addr(sV), Lay::kChunkBytes);
+    bool issued_any = false;
 
-      // S_t = Q_t K^T from key stage s.
-      auto issue_s = [&](int t, int s) {
+    // S_t = Q_t K^T from key stage s.
+    auto issue_s = [&](int t, int s) {
+      const uint32_t a0 = q_lo + static_cast<uint32_t>(t * (Lay::kTileBytes >> 4));
+      const uint32_t b0 = k_lo + static_cast<uint32_t>(s * (Lay::kTileBytes >> 4));
+      const uint32_t d = t ? tS[1] : tS[0];
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const int c = kk >> 2;           // which 64-wide chunk of D
-          const int koff = (kk & 3) * 32;  // 16 elements = 32 B inside the atom
-          const uint64_t adesc = smem_desc_sw128(
-              aQ + t * Lay::kTileBytes + c * Lay::kChunkBytes + koff, 16, 1024);
-          const uint64_t bdesc =
-              smem_desc_sw128(aK + s * Lay::kTileBytes + c * Lay::kChunkBytes + koff, 16, 1024);
-          mma_ss(tS[t], adesc, bdesc, idS, kk > 0 ? 1u : 0u);
-        }
-        mma_commit(&bars->s_full[t]);
-      };
-      // O_t (+)= P_t V from value stage s, P_t read from the first 64 columns of S_t.
-      auto issue_pv = [&](int t, int s, bool accumulate) {
+      for (int kk = 0; kk < D / 16; ++kk) {
+        // chunk of D (kk / 4), then 16 elements = 32 B inside the atom
+        const uint32_t off = ((kk >> 2) * Lay::kChunkBytes + (kk & 3) * 32) >> 4;
+        mma_ss_elect<kHiKMajor, kHiKMajor>(d, a0 + off, b0 + off, idS, kk > 0 ? 1u : 0u);
+      }
+      mma_commit_elect(&bars->s_full[t]);
+    };
+    // O_t (+)= P_t V from value stage s, P_t read from the first 64 columns of S_t.
+    auto issue_pv = [&](int t, int s, bool accumulate) {
+      const uint32_t b0 = v_lo + static_cast<uint32_t>(s * (Lay::kTileBytes >> 4));
+      const uint32_t d = t ? tO[1] : tO[0];
+      const uint32_t a = t ? tS[1] : tS[0];
 #pragma unroll
-        for (int kk = 0; kk < kBlockN / 16; ++kk) {
-          // V tile, keys kk*16 .. +16: rows of 128 B per 64-wide chunk of D,
-          // chunks one box apart (LBO), 8-row groups 1 KB apart (SBO).
-          const uint64_t bdesc = smem_desc_sw128(aV + s * Lay::kTileBytes + kk * 16 * 128,
-                                                 Lay::kChunkBytes, 1024);
-          mma_ts(tO[t], tS[t] + kk * 8, bdesc, idPV, (accumulate || kk > 0) ? 1u : 0u);
-        }
-        mma_commit(&bars->o_done[t]);
-      };
+      for (int kk = 0; kk < kBlockN / 16; ++kk) {
+        // keys kk*16 .. +16: 16 rows of 128 B
+        mma_ts_elect<kHiV>(d, a + kk * 8, b0 + ((kk * 16 * 128) >> 4), idPV,
+                           (accumulate || kk > 0) ? 1u : 0u);
+      }
+      mma_commit_elect(&bars->o_done[t]);
+    };
 
-      bool ok = wait_phase(&bars->q_full, 0, bars, limit, kSiteQFull) &&
-                wait_phase(&bars->k_full[0], 0, bars, limit, kSiteKFull);
-      if (ok) {
-        tc_fence_after();
+    bool ok = warp_wait_phase(&bars->q_full, 0, bars, limit, kSiteQFull) &&
+              warp_wait_phase(&bars->k_full[0], 0, bars, limit, kSiteKFull);
+    if (ok) {
+      tc_fence_after();
 #pragma unroll
-        for (int t = 0; t < kTilesPerCta; ++t)
-          if (w.n_kv[t] > 0) issue_s(t, 0);
-        mma_commit(&bars->k_empty[0]);
-        issued_any = true;
-        for (int j = 0; j < w.n_kv_max && ok; ++j) {
-          const int s = j % Lay::kStages;
-          const int s1 = (j + 1) % Lay::kStages;
-          if (!wait_phase(&bars->v_full[s], (j / Lay::kStages) & 1, bars, limit, kSiteVFull)) {
+      for (int t = 0; t < kTilesPerCta; ++t)
+        if (w.n_kv[t] > 0) issue_s(t, 0);
+      mma_commit_elect(&bars->k_empty[0]);
+      issued_any = true;
+      for (int j = 0; j < w.n_kv_max && ok; ++j) {
+        const int s = j % Lay::kStages;
+        const int s1 = (j + 1) % Lay::kStages;
+        if (!warp_wait_phase(&bars->v_full[s], (j / Lay::kStages) & 1, bars, limit,
+                             kSiteVFull)) {
+          ok = false;
+          break;
+        }
+        bool k_next = false;
+#pragma unroll
+        for (int t = 0; t < kTilesPerCta; ++t) {
+          if (j >= w.n_kv[t]) continue;
+          if (!warp_wait_phase(&bars->p_ready[t], j & 1, bars, limit, kSitePReady)) {
             ok = false;
             break;
           }
-          bool k_next = false;
-#pragma unroll
-          for (int t = 0; t < kTilesPerCta; ++t) {
-            if (j >= w.n_kv[t]) continue;
-            if (!wait_phase(&bars->p_ready[t], j & 1, bars, limit, kSitePReady)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            issue_pv(t, s, j > 0);
-            if (j + 1 < w.n_kv[t]) {
-              if (!k_next) {
-                if (!wait_phase(&bars->k_full[s1], ((j + 1) / Lay::kStages) & 1, bars, limit,
-                                kSiteKFull)) {
-                  ok = false;
-                  break;
-                }
-                tc_fence_after();
-                k_next = true;
+          tc_fence_after();
+          issue_pv(t, s, j > 0);
+          if (j + 1 < w.n_kv[t]) {
+            if (!k_next) {
+              if (!warp_wait_phase(&bars->k_full[s1], ((j + 1) / Lay::kStages) & 1, bars, limit,
+                                   kSiteKFull)) {
+                ok = false;
+                break;
               }
-              issue_s(t, s1);
+              tc_fence_after();
+              k_next = true;
             }
+            issue_s(t, s1);
           }
-          if (!ok) break;
-          mma_commit(&bars->v_empty[s]);
-          if (k_next) mma_commit(&bars->k_empty[s1]);
         }
+        if (!ok) break;
+        mma_commit_elect(&bars->v_empty[s]);
+        if (k_next) mma_commit_elect(&bars->k_empty[s1]);
       }
-      if (issued_any) {
-        // Everything issued must finish before TMEM is released.
-        mma_commit(&bars->fin);
-        wait_phase(&bars->fin, 0, bars, limit, kSiteDrain, false);
-      }
+    }
+    if (issued_any) {
+      // Everything issued must finish before TMEM is released.
+      mma_commit_elect(&bars->fin);
+      wait_phase(&bars->fin, 0, bars, limit, kSiteDrain, false);
     }
   }
   }  // control warpgroup
