@@ -312,6 +312,17 @@ __device__ __forceinline__ void fma2_bcast(float& o0, float& o1, float a0, float
       : "=f"(o0), "=f"(o1)
       : "f"(a0), "f"(a1), "f"(b), "f"(c));
 }
+// (q0, q1) = (q0, q1) * (f0, f1) + c (c broadcast)
+__device__ __forceinline__ void fma2_mul_add(float& q0, float& q1, float f0, float f1, float c) {
+  asm("{\n\t.reg .b64 rq, rf, rc;\n\t"
+      "mov.b64 rq, {%0, %1};\n\t"
+      "mov.b64 rf, {%2, %3};\n\t"
+      "mov.b64 rc, {%4, %4};\n\t"
+      "fma.rn.f32x2 rq, rq, rf, rc;\n\t"
+      "mov.b64 {%0, %1}, rq;\n\t}"
+      : "+f"(q0), "+f"(q1)
+      : "f"(f0), "f"(f1), "f"(c));
+}
 // (a0, a1) += (b0, b1)
 __device__ __forceinline__ void add2_acc(float& a0, float& a1, float b0, float b1) {
   asm("{\n\t.reg .b64 ra, rb;\n\t"
@@ -332,6 +343,38 @@ __device__ __forceinline__ void mul2_bcast(float& a0, float& a1, float b) {
       : "+f"(a0), "+f"(a1)
       : "f"(b));
 }
+// Base-2 exponential of two values on the FMA/ALU pipes instead of MUFU
+// (Cody-Waite range reduction plus a minimax cubic).  2^x = 2^n * 2^f with
+// n = round(x) taken by adding 1.5 * 2^23 (the sum's low mantissa bits hold
+// n), f = x - n in [-1/2, 1/2], and 2^f ~ 1 + f (c1 + f (c2 + f c3)); 2^n is
+// applied by adding n to the exponent field.  Inputs below -127 are clamped
+// to -127, which returns exactly +0.0 (c0 = 1 exactly), so removed scores
+// (-inf) still give probability 0.  Maximum relative error 1.02e-4 on the
+// whole range; c1..c3 come from scaled_dot_product_forward_gb300/
+// fit_exp2_poly.py (a minimax fit solved as a linear program).
+constexpr float kExp2C1 = 6.932829022e-01f;  // 0x3f317afd
+constexpr float kExp2C2 = 2.422109693e-01f;  // 0x3e780627
+constexpr float kExp2C3 = 5.500905961e-02f;  // 0x3d61512e
+
+__device__ __forceinline__ void ex2_poly2(float& y0, float& y1, float x0, float x1) {
+  constexpr float kRound = 12582912.0f;  // 1.5 * 2^23
+  x0 = fmaxf(x0, -127.0f);
+  x1 = fmaxf(x1, -127.0f);
+  float t0 = x0, t1 = x1;
+  add2_acc(t0, t1, kRound, kRound);  // t = x + 1.5*2^23: rounds x to an integer
+  float n0 = t0, n1 = t1;
+  add2_acc(n0, n1, -kRound, -kRound);  // n = round(x) as a float
+  float f0 = -n0, f1 = -n1;
+  add2_acc(f0, f1, x0, x1);  // f = x - n
+  float q0, q1;
+  fma2_bcast(q0, q1, f0, f1, kExp2C3, kExp2C2);  // c3 f + c2
+  fma2_mul_add(q0, q1, f0, f1, kExp2C1);        // (.) f + c1
+  fma2_mul_add(q0, q1, f0, f1, 1.0f);           // (.) f + 1
+  // add n (the low bits of t) to the exponent field
+  y0 = __int_as_float(__float_as_int(t0) * (1 << 23) + __float_as_int(q0));
+  y1 = __int_as_float(__float_as_int(t1) * (1 << 23) + __float_as_int(q1));
+}
+
 // Three-input maximum / minimum.
 __device__ __forceinline__ float max3f(float a, float b, float c) {
   float d;

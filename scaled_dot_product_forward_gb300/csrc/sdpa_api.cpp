@@ -285,6 +285,16 @@ void sdpa_debug_set_wait_limit_ns(uint64_t ns) {
   g_wait_limit_ns.store(ns == 0 ? kDefaultWaitLimitNs : ns, std::memory_order_relaxed);
 }
 
+sdpa_status sdpa_debug_exp2_poly(const float* x, float* y, int64_t n, void* stream) {
+  if (!x || !y) return SDPA_ERR_NULL;
+  if (n < 0 || n > (int64_t(1) << 31)) return SDPA_ERR_SHAPE;
+  const sdpa_status s = check_device();
+  if (s != SDPA_OK) return s;
+  return sdpa_impl::launch_exp2_poly(x, y, n, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? SDPA_OK
+             : SDPA_ERR_CUDA;
+}
+
 void sdpa_debug_withhold_q_load(int enable) {
   g_withhold_q.store(enable ? 1 : 0, std::memory_order_relaxed);
 }

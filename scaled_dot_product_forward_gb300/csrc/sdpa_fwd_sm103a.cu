@@ -58,6 +58,12 @@ constexpr uint32_t kRegsSoftmax = 224;
 static_assert(128 * kRegsControl + 256 * kRegsSoftmax <= kThreads * kLaunchRegs,
               "register split exceeds the launch allocation");
 constexpr float kRescaleLog2 = 8.0f;  // rescale O only when max grows by > 2^8
+// When nonzero, one pair of exponentials in every kPolyPeriod goes through
+// the FMA-pipe polynomial instead of MUFU.  Off: on GB300 the exponential
+// unit is not the binding limit of this loop (offloading a quarter of the
+// pairs lowered the [4,32,4096,128] causal rate from 1235 to 1177 TFLOP/s,
+// the extra instructions costing more issue slots than MUFU time saved).
+constexpr int kPolyPeriod = 0;
 constexpr uint32_t kTmemCols = 512;
 
 enum WaitSite : unsigned int {
@@ -210,6 +216,49 @@ __device__ __forceinline__ void softmax_role(const sdpa_impl::FwdParams& p, cons
   bool ok = true;
 
   for (int j = 0; j < n; ++j) {
+    const int col0 = j * kBlockN;
+    const bool tail = col0 + kBlockN > p.L;
+    const bool masked_tile = (MODE == sdpa_impl::kMaskExplicit) || tail ||
+                             (MODE == sdpa_impl::kMaskCausal && j == qt);
+    // Explicit mask: this row's 128 mask bytes for tile j, one bit per key
+    // (bit set = removed).  Loaded before waiting for S so their latency
+    // hides behind the score MMA.
+    uint32_t mbits[kBlockN / 32];
+    if constexpr (MODE == sdpa_impl::kMaskExplicit) {
+      const bool row_ok = row_g < p.L;
+      const uint8_t* mrow = p.mask + static_cast<int64_t>(row_ok ? row_g : 0) * p.L + col0;
+      if (p.mask_vec16 && !tail && row_ok) {
+        uint4 x[kBlockN / 16];
+#pragma unroll
+        for (int v = 0; v < kBlockN / 16; ++v) x[v] = __ldg(reinterpret_cast<const uint4*>(mrow) + v);
+#pragma unroll
+        for (int w32 = 0; w32 < kBlockN / 32; ++w32) {
+          uint32_t bits = 0;
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const uint4 xv = x[(32 * w32 + e) >> 4];
+            const int byte_in_v = (32 * w32 + e) & 15;
+            const uint32_t word = (byte_in_v < 4)    ? xv.x
+                                  : (byte_in_v < 8)  ? xv.y
+                                  : (byte_in_v < 12) ? xv.z
+                                                     : xv.w;
+            bits |= (((word >> (8 * (byte_in_v & 3))) & 0xffu) != 0u ? 1u : 0u) << e;
+          }
+          mbits[w32] = bits;
+        }
+      } else {
+#pragma unroll
+        for (int w32 = 0; w32 < kBlockN / 32; ++w32) {
+          uint32_t bits = 0;
+          for (int e = 0; e < 32; ++e) {
+            const int c = 32 * w32 + e;
+            const bool removed = !row_ok || col0 + c >= p.L || __ldg(mrow + c) != 0;
+            bits |= (removed ? 1u : 0u) << e;
+          }
+          mbits[w32] = bits;
+        }
+      }
+    }
     if (!warp_wait_phase(&bars->s_full[t], j & 1, bars, limit, kSiteSFull)) {
       ok = false;
       break;
@@ -224,45 +273,11 @@ __device__ __forceinline__ void softmax_role(const sdpa_impl::FwdParams& p, cons
 #pragma unroll
       for (int c = 0; c < kBlockN; ++c) s[c] = __uint_as_float(su[c]);
     }
-    const int col0 = j * kBlockN;
-    const bool tail = col0 + kBlockN > p.L;
-    const bool masked_tile = (MODE == sdpa_impl::kMaskExplicit) || tail ||
-                             (MODE == sdpa_impl::kMaskCausal && j == qt);
     if (masked_tile) {
       if constexpr (MODE == sdpa_impl::kMaskExplicit) {
-        const bool row_ok = row_g < p.L;
-        const uint8_t* mrow = p.mask + static_cast<int64_t>(row_ok ? row_g : 0) * p.L + col0;
-        const bool vec = p.mask_vec16 && !tail && row_ok;
 #pragma unroll
-        for (int v = 0; v < kBlockN / 16; ++v) {
-          uint32_t mw[4];
-          if (vec) {
-            const uint4 x = __ldg(reinterpret_cast<const uint4*>(mrow) + v);
-            mw[0] = x.x;
-            mw[1] = x.y;
-            mw[2] = x.z;
-            mw[3] = x.w;
-          } else {
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-              uint32_t word = 0;
-#pragma unroll
-              for (int b = 0; b < 4; ++b) {
-                const int c = 16 * v + 4 * q4 + b;
-                const uint32_t byte = (row_ok && col0 + c < p.L) ? __ldg(mrow + c) : 1u;
-                word |= (byte != 0 ? 1u : 0u) << (8 * b);
-              }
-              mw[q4] = word;
-            }
-          }
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const int c = 16 * v + e;
-            const bool removed =
-                (col0 + c >= p.L) || (((mw[e >> 2] >> (8 * (e & 3))) & 0xffu) != 0u);
-            s[c] = removed ? mval : s[c];
-          }
-        }
+        for (int c = 0; c < kBlockN; ++c)
+          s[c] = ((mbits[c >> 5] >> (c & 31)) & 1u) ? mval : s[c];
       } else {
 #pragma unroll
         for (int c = 0; c < kBlockN; ++c) {
@@ -308,21 +323,31 @@ __device__ __forceinline__ void softmax_role(const sdpa_impl::FwdParams& p, cons
     }
     const float neg_m = (m_used == -INFINITY) ? 0.0f : -m_used;
 
+    // Three passes over the row so each pass is a long run of independent
+    // instructions: x = s * scale*log2(e) - m (packed FMA), p = 2^x, then the
+    // packed row sums and the 16-bit packing.  A removed score is +-inf with
+    // the sign that makes x = -inf, so its probability is exactly 0 (the
+    // multiplier is never 0: the host maps a zero scale to +-FLT_MIN, which
+    // gives the same all-ones weights).
+#pragma unroll
+    for (int c = 0; c < kBlockN; c += 2) fma2_bcast(s[c], s[c + 1], s[c], s[c + 1], sl2, neg_m);
+#pragma unroll
+    for (int c = 0; c < kBlockN; c += 2) {
+      if (kPolyPeriod > 0 && (c / 2) % kPolyPeriod == kPolyPeriod - 1) {
+        ex2_poly2(s[c], s[c + 1], s[c], s[c + 1]);
+      } else {
+        s[c] = ex2(s[c]);
+        s[c + 1] = ex2(s[c + 1]);
+      }
+    }
     uint32_t pk[kBlockN / 2];
     float rs[8];  // four packed pairs of partial row sums
 #pragma unroll
     for (int i = 0; i < 8; ++i) rs[i] = 0.0f;
 #pragma unroll
     for (int c = 0; c < kBlockN / 2; ++c) {
-      // A removed score is +-inf with the sign that makes s * sl2 = -inf, so
-      // its probability is exactly 0 (sl2 is never 0: the host maps a zero
-      // scale to +-FLT_MIN, which gives the same all-ones weights).
-      float x0, x1;
-      fma2_bcast(x0, x1, s[2 * c], s[2 * c + 1], sl2, neg_m);
-      const float p0 = ex2(x0);
-      const float p1 = ex2(x1);
-      add2_acc(rs[2 * (c & 3)], rs[2 * (c & 3) + 1], p0, p1);
-      pk[c] = pack2<BF16>(p0, p1);
+      add2_acc(rs[2 * (c & 3)], rs[2 * (c & 3) + 1], s[2 * c], s[2 * c + 1]);
+      pk[c] = pack2<BF16>(s[2 * c], s[2 * c + 1]);
     }
     // P_j overwrites the first 64 columns of this tile's score buffer.
     tmem_st32(tS + 0, pk);
@@ -355,7 +380,8 @@ __device__ __forceinline__ void softmax_role(const sdpa_impl::FwdParams& p, cons
     }
     tmem_st_wait();
     tc_fence_before();
-    mbar_arrive(&bars->p_ready[t]);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bars->p_ready[t]);  // one arrival per warp
   }
 
   if (ok && warp_wait_phase(&bars->o_done[t], (n - 1) & 1, bars, limit, kSiteODone)) {
@@ -407,7 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
     for (int t = 0; t < kTilesPerCta; ++t) {
       mbar_init(&bars->s_full[t], 1);
-      mbar_init(&bars->p_ready[t], kBlockM);
+      mbar_init(&bars->p_ready[t], kBlockM / 32);
       mbar_init(&bars->o_done[t], 1);
     }
     mbar_init(&bars->fin, 1);
@@ -636,9 +662,32 @@ cudaError_t launch_mode(const sdpa_impl::FwdParams& p, int mode, cudaStream_t st
   }
 }
 
+// Test hook: y = 2^x through the FMA-pipe polynomial (pairs of elements).
+__global__ void exp2_poly_kernel(const float* x, float* y, int64_t n) {
+  const int64_t i = 2 * (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x);
+  if (i + 1 < n) {
+    float a, b;
+    ex2_poly2(a, b, x[i], x[i + 1]);
+    y[i] = a;
+    y[i + 1] = b;
+  } else if (i < n) {
+    float a, b;
+    ex2_poly2(a, b, x[i], 0.0f);
+    y[i] = a;
+  }
+}
+
 }  // namespace
 
 namespace sdpa_impl {
+
+cudaError_t launch_exp2_poly(const float* x, float* y, int64_t n, cudaStream_t stream) {
+  if (n <= 0) return cudaSuccess;
+  const int64_t pairs = (n + 1) / 2;
+  const unsigned blocks = static_cast<unsigned>((pairs + 255) / 256);
+  exp2_poly_kernel<<<blocks, 256, 0, stream>>>(x, y, n);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_forward(const FwdParams& p, int head_dim, int mask_mode, bool bf16,
                            cudaStream_t stream) {

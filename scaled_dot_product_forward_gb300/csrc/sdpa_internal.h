@@ -32,6 +32,9 @@ enum MaskMode : int { kMaskNone = 0, kMaskCausal = 1, kMaskExplicit = 2 };
 cudaError_t launch_forward(const FwdParams& p, int head_dim, int mask_mode, bool bf16,
                            cudaStream_t stream);
 
+// Test hook: y[i] = 2^x[i] through the kernel's FMA-pipe polynomial.
+cudaError_t launch_exp2_poly(const float* x, float* y, int64_t n, cudaStream_t stream);
+
 // Reads and clears the device status word (nonzero = a barrier wait timed out).
 cudaError_t read_and_clear_device_status(cudaStream_t stream, unsigned int* status);
 
