@@ -58,12 +58,33 @@ constexpr uint32_t kRegsSoftmax = 224;
 static_assert(128 * kRegsControl + 256 * kRegsSoftmax <= kThreads * kLaunchRegs,
               "register split exceeds the launch allocation");
 constexpr float kRescaleLog2 = 8.0f;  // rescale O only when max grows by > 2^8
+
+// With D = 64 the two output accumulators take only 128 TMEM columns, which
+// leaves room for P in its own 64-column buffers.  Then S(j+1) no longer has
+// to wait for PV(j) to consume P(j): it is issued as soon as the softmax has
+// loaded S(j) into registers, and each softmax warpgroup runs tile after
+// tile without waiting for its own products.  With D = 128 the 512 columns
+// are all used (S_A, S_B, O_A, O_B) and P is written over S.
+template <int D>
+struct TmemPlan {
+  static constexpr bool kEarlyS = (D == 64);
+  __host__ __device__ static constexpr uint32_t s_col(int t) { return t ? 128u : 0u; }
+  __host__ __device__ static constexpr uint32_t o_col(int t) { return t ? 256u + D : 256u; }
+  __host__ __device__ static constexpr uint32_t p_col(int t) {
+    return kEarlyS ? (t ? 256u + 2 * D + 64 : 256u + 2 * D) : s_col(t);
+  }
+  static_assert(!kEarlyS || 256 + 2 * D + 128 <= 512, "TMEM plan exceeds 512 columns");
+};
+
 // When nonzero, one pair of exponentials in every kPolyPeriod goes through
 // the FMA-pipe polynomial instead of MUFU.  Off: on GB300 the exponential
 // unit is not the binding limit of this loop (offloading a quarter of the
 // pairs lowered the [4,32,4096,128] causal rate from 1235 to 1177 TFLOP/s,
 // the extra instructions costing more issue slots than MUFU time saved).
 constexpr int kPolyPeriod = 0;
+__host__ __device__ constexpr bool poly_pair(int pair) {
+  return kPolyPeriod > 0 && pair % (kPolyPeriod > 0 ? kPolyPeriod : 1) == kPolyPeriod - 1;
+}
 constexpr uint32_t kTmemCols = 512;
 
 enum WaitSite : unsigned int {
@@ -75,6 +96,7 @@ enum WaitSite : unsigned int {
   kSiteODone = 1u << 6,
   kSiteDrain = 1u << 7,
   kSiteVFull = 1u << 8,
+  kSiteSFree = 1u << 9,
 };
 
 template <int D>
@@ -97,6 +119,7 @@ struct Barriers {
   uint64_t s_full[kTilesPerCta];
   uint64_t p_ready[kTilesPerCta];
   uint64_t o_done[kTilesPerCta];
+  uint64_t s_free[kTilesPerCta];  // S(j) loaded by the softmax (early-S plan only)
   uint64_t fin;
   uint64_t k_full[kMaxStages];
   uint64_t v_full[kMaxStages];
@@ -201,8 +224,11 @@ __device__ __forceinline__ void softmax_role(const sdpa_impl::FwdParams& p, cons
   if (n == 0) return;
   const uint64_t limit = p.wait_limit_ns;
   const int qt = t ? w.tile[1] : w.tile[0];
-  const uint32_t tS_base = tmem + (t ? 128u : 0u);
-  const uint32_t tO_base = tmem + 256u + (t ? static_cast<uint32_t>(D) : 0u);
+  using Plan = TmemPlan<D>;
+  const uint32_t tS_base = tmem + (t ? Plan::s_col(1) : Plan::s_col(0));
+  const uint32_t tO_base = tmem + (t ? Plan::o_col(1) : Plan::o_col(0));
+  const uint32_t tP =
+      tmem + (t ? Plan::p_col(1) : Plan::p_col(0)) + (static_cast<uint32_t>(wq * 32) << 16);
   const int r = wq * 32 + lane;
   const int row_g = qt * kBlockM + r;
   const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
@@ -273,6 +299,12 @@ __device__ __forceinline__ void softmax_role(const sdpa_impl::FwdParams& p, cons
 #pragma unroll
       for (int c = 0; c < kBlockN; ++c) s[c] = __uint_as_float(su[c]);
     }
+    if constexpr (Plan::kEarlyS) {
+      // S(j) is in registers: the MMA warp may overwrite it with S(j+1).
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->s_free[t]);
+    }
     if (masked_tile) {
       if constexpr (MODE == sdpa_impl::kMaskExplicit) {
 #pragma unroll
@@ -333,7 +365,7 @@ __device__ __forceinline__ void softmax_role(const sdpa_impl::FwdParams& p, cons
     for (int c = 0; c < kBlockN; c += 2) fma2_bcast(s[c], s[c + 1], s[c], s[c + 1], sl2, neg_m);
 #pragma unroll
     for (int c = 0; c < kBlockN; c += 2) {
-      if (kPolyPeriod > 0 && (c / 2) % kPolyPeriod == kPolyPeriod - 1) {
+      if (poly_pair(c / 2)) {
         ex2_poly2(s[c], s[c + 1], s[c], s[c + 1]);
       } else {
         s[c] = ex2(s[c]);
@@ -349,17 +381,17 @@ __device__ __forceinline__ void softmax_role(const sdpa_impl::FwdParams& p, cons
       add2_acc(rs[2 * (c & 3)], rs[2 * (c & 3) + 1], s[2 * c], s[2 * c + 1]);
       pk[c] = pack2<BF16>(s[2 * c], s[2 * c + 1]);
     }
-    // P_j overwrites the first 64 columns of this tile's score buffer.
-    tmem_st32(tS + 0, pk);
-    tmem_st32(tS + 32, pk + 32);
     add2_acc(rs[0], rs[1], rs[2], rs[3]);
     add2_acc(rs[4], rs[5], rs[6], rs[7]);
     add2_acc(rs[0], rs[1], rs[4], rs[5]);
     l += rs[0] + rs[1];
 
     if (j > 0) {
-      // Consume PV_{j-1}'s completion in order (keeps phase parity exact);
-      // it is needed anyway before O may be rescaled.
+      // Consume PV_{j-1}'s completion in order; it is needed anyway before O
+      // may be rescaled.  This wait must stay BEFORE the p_ready arrival
+      // below: once P_j is released, PV_j may complete too, and a parity
+      // wait that falls two phases behind its barrier would block until the
+      // next phase (a timeout here) instead of returning.
       if (!warp_wait_phase(&bars->o_done[t], (j - 1) & 1, bars, limit, kSiteODone)) {
         ok = false;
         break;
@@ -378,6 +410,11 @@ __device__ __forceinline__ void softmax_role(const sdpa_impl::FwdParams& p, cons
         }
       }
     }
+    // P_j goes into the P buffer -- the first 64 columns of this tile's score
+    // buffer, or its own buffer in the early-S plan (free again: PV_{j-1}
+    // has completed, waited for above).
+    tmem_st32(tP + 0, pk);
+    tmem_st32(tP + 32, pk + 32);
     tmem_st_wait();
     tc_fence_before();
     __syncwarp();
@@ -435,6 +472,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->s_full[t], 1);
       mbar_init(&bars->p_ready[t], kBlockM / 32);
       mbar_init(&bars->o_done[t], 1);
+      mbar_init(&bars->s_free[t], kBlockM / 32);
     }
     mbar_init(&bars->fin, 1);
 #pragma unroll
@@ -460,9 +498,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
-  // TMEM columns: S_A [0,128), S_B [128,256), O_A [256, 256+D), O_B [256+D, 256+2D)
-  const uint32_t tS[kTilesPerCta] = {tmem, tmem + 128};
-  const uint32_t tO[kTilesPerCta] = {tmem + 256, tmem + 256 + D};
+  // TMEM columns: S_A [0,128), S_B [128,256), O_A [256, 256+D), O_B [256+D, 256+2D),
+  // and with D = 64 also P_A [384, 448), P_B [448, 512).
+  using Plan = TmemPlan<D>;
+  const uint32_t tS[kTilesPerCta] = {tmem + Plan::s_col(0), tmem + Plan::s_col(1)};
+  const uint32_t tO[kTilesPerCta] = {tmem + Plan::o_col(0), tmem + Plan::o_col(1)};
+  const uint32_t tPv[kTilesPerCta] = {tmem + Plan::p_col(0), tmem + Plan::p_col(1)};
 
   if (warp >= 4) {
     // ------------------------------------------- softmax / output warps
@@ -552,11 +593,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       mma_commit_elect(&bars->s_full[t]);
     };
-    // O_t (+)= P_t V from value stage s, P_t read from the first 64 columns of S_t.
+    // O_t (+)= P_t V from value stage s, P_t read from TMEM (keys 2c, 2c+1 in column c).
     auto issue_pv = [&](int t, int s, bool accumulate) {
       const uint32_t b0 = v_lo + static_cast<uint32_t>(s * (Lay::kTileBytes >> 4));
       const uint32_t d = t ? tO[1] : tO[0];
-      const uint32_t a = t ? tS[1] : tS[0];
+      const uint32_t a = t ? tPv[1] : tPv[0];
 #pragma unroll
       for (int kk = 0; kk < kBlockN / 16; ++kk) {
         // keys kk*16 .. +16: 16 rows of 128 B
@@ -578,12 +619,53 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < w.n_kv_max && ok; ++j) {
         const int s = j % Lay::kStages;
         const int s1 = (j + 1) % Lay::kStages;
+        bool k_next = false;
+        if constexpr (Plan::kEarlyS) {
+          // S(j+1) of both tiles first (each once its softmax has loaded
+          // S(j)), then PV(j) of both tiles as their P(j) become ready.
+#pragma unroll
+          for (int t = 0; t < kTilesPerCta; ++t) {
+            if (j + 1 >= w.n_kv[t]) continue;
+            if (!k_next) {
+              if (!warp_wait_phase(&bars->k_full[s1], ((j + 1) / Lay::kStages) & 1, bars, limit,
+                                   kSiteKFull)) {
+                ok = false;
+                break;
+              }
+              k_next = true;
+            }
+            if (!warp_wait_phase(&bars->s_free[t], j & 1, bars, limit, kSiteSFree)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_s(t, s1);
+          }
+          if (!ok) break;
+          if (k_next) mma_commit_elect(&bars->k_empty[s1]);
+          if (!warp_wait_phase(&bars->v_full[s], (j / Lay::kStages) & 1, bars, limit,
+                               kSiteVFull)) {
+            ok = false;
+            break;
+          }
+#pragma unroll
+          for (int t = 0; t < kTilesPerCta; ++t) {
+            if (j >= w.n_kv[t]) continue;
+            if (!warp_wait_phase(&bars->p_ready[t], j & 1, bars, limit, kSitePReady)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_pv(t, s, j > 0);
+          }
+          if (!ok) break;
+          mma_commit_elect(&bars->v_empty[s]);
+        } else {
         if (!warp_wait_phase(&bars->v_full[s], (j / Lay::kStages) & 1, bars, limit,
                              kSiteVFull)) {
           ok = false;
           break;
         }
-        bool k_next = false;
 #pragma unroll
         for (int t = 0; t < kTilesPerCta; ++t) {
           if (j >= w.n_kv[t]) continue;
@@ -609,6 +691,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         mma_commit_elect(&bars->v_empty[s]);
         if (k_next) mma_commit_elect(&bars->k_empty[s1]);
+        }  // plan with P written over S
       }
     }
     if (issued_any) {
