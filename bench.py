@@ -210,13 +210,43 @@ def gpu_leg(args, w, rank, world):
     def step():
         sdpa.sdpa_forward(qd, kd, vd, out, is_causal=w.is_causal, mask=md, stream=stream)
 
+    plan = sdpa.SdpaPlan(qd, kd, vd, out, is_causal=w.is_causal, mask=md)
+
+    def plan_step():
+        plan.launch(stream)
+
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
             step()
+            plan_step()
     stream.synchronize()
     rc, detail = sdpa.sdpa_last_device_status(stream)
     if rc != 0:
         raise RuntimeError(f"warm-up reported {sdpa.sdpa_status_string(rc)} ({detail:#x})")
+
+    # Host cost of one call (no synchronisation inside; the GPU queue absorbs
+    # the launches), through the one-shot entry point and through a plan.
+    host_us = {}
+    for name, fn in (("sdpa_forward", step), ("plan_launch", plan_step)):
+        n = 64
+        stream.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(n):
+            fn()
+        host_us[name] = (time.perf_counter() - t0) / n * 1e6
+        stream.synchronize()
+
+    graph = None
+    if args.graph:
+        # K plan launches captured once; the timed region replays them with
+        # no host work between kernels.
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for _ in range(args.steps):
+                plan.launch(stream)
+        with torch.cuda.stream(stream):
+            graph.replay()
+        stream.synchronize()
 
     # --- timed region: K launches, an event pair around each one
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
@@ -229,17 +259,24 @@ def gpu_leg(args, w, rank, world):
     clocks.start()
     time.sleep(0.3)  # let the sampler start before the work
     t_begin.record(stream)
-    for i in range(args.steps):
-        starts[i].record(stream)
-        step()
-        ends[i].record(stream)
+    if graph is not None:
+        with torch.cuda.stream(stream):  # replay() launches on the current stream
+            graph.replay()
+    else:
+        for i in range(args.steps):
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
     t_end.record(stream)
     torch.cuda.synchronize(dev)
     clk = clocks.stop()
     if world > 1:
         torch.distributed.barrier()
     total_ms = t_begin.elapsed_time(t_end)
-    per_launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    if graph is not None:
+        per_launch_ms = [total_ms / args.steps]  # back to back, no host gaps
+    else:
+        per_launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     rc, detail = sdpa.sdpa_last_device_status(stream)
     if rc != 0:
         raise RuntimeError(f"timed region reported {sdpa.sdpa_status_string(rc)} ({detail:#x})")
@@ -273,8 +310,9 @@ def gpu_leg(args, w, rank, world):
     h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv)) + (
         hm.numel() if hm is not None else 0)
     d2h = hout.numel() * hout.element_size()
+    plan.close()
     return dict(total_ms=total_ms, per_launch_ms=per_launch_ms, clocks=clk, e2e_ms=e2e_ms,
-                h2d=h2d, d2h=d2h, flops=flops)
+                h2d=h2d, d2h=d2h, flops=flops, host_us=host_us)
 
 
 def max_over_ranks(x: float, world: int) -> float:
@@ -298,6 +336,8 @@ def main(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--graph", action="store_true",
+                    help="time a CUDA graph of K plan launches (no host gaps between kernels)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -307,6 +347,7 @@ def main(argv=None):
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     config = {"workload": w.name, "B": w.B, "H": w.H, "L": w.L, "D": w.D,
+              "launch": "cuda graph of plan launches" if args.graph else "sdpa_forward per step",
               "is_causal": w.is_causal, "mask": w.p_masked is not None,
               "rank": w.rank, "scale": "1/sqrt(D)",
               "l2": "no flush: q, k, v, out total %.0f MB > 129 MB L2" % (
@@ -367,6 +408,7 @@ def main(argv=None):
                     "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"],
                     "ms_per_step": e2e_ms},
             "gpu_launches": args.steps,
+            "host_us_per_call": r["host_us"],
             "clocks": r["clocks"]}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         sampler = OracleSampler(w)

@@ -27,7 +27,10 @@
  *     kernels", daker.dacon.io, sections on the rank-3 problem and on what
  *     changed in 2.14); results are bit-identical to the rank-4 call.
  *
- * Computation: one GPU kernel launch per call; 16-bit inputs on tensor cores
+ * Computation: one GPU kernel launch per call, launched with programmatic
+ * stream serialization (its set-up overlaps the previous kernel in the
+ * stream, its first global-memory access waits for that kernel); 16-bit
+ * inputs on tensor cores
  * with fp32 accumulation, the softmax in fp32, probabilities rounded to the
  * input type before the second product, output rounded to nearest even.
  */
@@ -102,6 +105,47 @@ SDPA_API sdpa_status sdpa_forward(const void* q, const void* k, const void* v, v
                          const int64_t* q_stride, const int64_t* k_stride,
                          const int64_t* v_stride, const int64_t* o_stride,
                          int is_causal, const uint8_t* mask, float scale, void* stream);
+
+/*
+ * Plans -- validate and encode once, launch many times.
+ *
+ * sdpa_forward validates its arguments and encodes three TMA descriptors on
+ * every call.  A plan does that work once for a fixed shape, dtype, strides,
+ * mask mode and scale (the same arguments and the same errors as
+ * sdpa_forward); sdpa_plan_launch then only launches the kernel, which keeps
+ * the host cost of a call to a few microseconds.  (The pages measure 117-214
+ * us of CPU time per forward for the fused PyTorch backends, most of it
+ * per-call plan selection for cuDNN: "Profiling attention in PyTorch:
+ * kernels, backends and where the time goes", news.bpdata.com, section
+ * "cuDNN backend".)
+ *
+ * sdpa_plan_create      : *plan receives a new plan (host memory owned by the
+ *                         caller until sdpa_plan_destroy), or NULL on error.
+ *                         Binds the plan to the current device.
+ * sdpa_plan_set_pointers: rebinds q, k, v, out (and mask, which must be
+ *                         present iff it was at creation) to new DEVICE
+ *                         buffers of the same shape and strides; validated
+ *                         like sdpa_forward.  Not thread-safe with a
+ *                         concurrent launch of the same plan.
+ * sdpa_plan_launch      : enqueues the forward on `stream` (asynchronous);
+ *                         SDPA_ERR_ARG if the current device is not the
+ *                         plan's.  Safe to call from several threads on
+ *                         different streams, and inside CUDA graph capture.
+ * sdpa_plan_destroy     : frees the plan (NULL is ignored).  Work already
+ *                         enqueued is unaffected.
+ */
+typedef struct sdpa_plan sdpa_plan;
+
+SDPA_API sdpa_status sdpa_plan_create(sdpa_plan** plan, const void* q, const void* k,
+                                      const void* v, void* out, sdpa_dtype dtype, int rank,
+                                      const int64_t* shape, const int64_t* q_stride,
+                                      const int64_t* k_stride, const int64_t* v_stride,
+                                      const int64_t* o_stride, int is_causal,
+                                      const uint8_t* mask, float scale);
+SDPA_API sdpa_status sdpa_plan_set_pointers(sdpa_plan* plan, const void* q, const void* k,
+                                            const void* v, void* out, const uint8_t* mask);
+SDPA_API sdpa_status sdpa_plan_launch(const sdpa_plan* plan, void* stream);
+SDPA_API void sdpa_plan_destroy(sdpa_plan* plan);
 
 /* Human-readable name of a status code (static storage, never NULL). */
 SDPA_API const char* sdpa_status_string(sdpa_status status);

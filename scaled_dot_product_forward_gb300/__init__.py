@@ -19,7 +19,8 @@ from . import _build
 
 __all__ = ["sdpa_forward", "sdpa_forward_raw", "sdpa_status_string", "sdpa_last_device_status",
            "sdpa_version", "SdpaError", "load_library", "LIB_PATH", "STATUS",
-           "sdpa_debug_set_wait_limit_ns", "sdpa_debug_withhold_q_load", "sdpa_debug_exp2_poly"]
+           "sdpa_debug_set_wait_limit_ns", "sdpa_debug_withhold_q_load", "sdpa_debug_exp2_poly",
+           "SdpaPlan"]
 
 LIB_PATH = _build.LIB_PATH
 
@@ -67,6 +68,16 @@ def load_library(path: str | None = None):
     lib.sdpa_debug_withhold_q_load.restype = None
     lib.sdpa_debug_exp2_poly.argtypes = [vp, vp, ctypes.c_int64, vp]
     lib.sdpa_debug_exp2_poly.restype = ctypes.c_int
+    lib.sdpa_plan_create.argtypes = [ctypes.POINTER(vp), vp, vp, vp, vp, ctypes.c_int,
+                                     ctypes.c_int, i64p, i64p, i64p, i64p, i64p, ctypes.c_int,
+                                     vp, ctypes.c_float]
+    lib.sdpa_plan_create.restype = ctypes.c_int
+    lib.sdpa_plan_set_pointers.argtypes = [vp, vp, vp, vp, vp, vp]
+    lib.sdpa_plan_set_pointers.restype = ctypes.c_int
+    lib.sdpa_plan_launch.argtypes = [vp, vp]
+    lib.sdpa_plan_launch.restype = ctypes.c_int
+    lib.sdpa_plan_destroy.argtypes = [vp]
+    lib.sdpa_plan_destroy.restype = None
     if path is None:
         _lib = lib
     return lib
@@ -161,6 +172,74 @@ def sdpa_forward(q, k, v, out=None, *, is_causal: bool = False, mask=None, scale
     if rc != 0:
         raise SdpaError(rc)
     return out
+
+
+def _dtype_code(q):
+    import torch
+    if q.dtype == torch.bfloat16:
+        return SDPA_BF16
+    if q.dtype == torch.float16:
+        return SDPA_FP16
+    raise SdpaError(4)
+
+
+def _mask_ptr(mask):
+    import torch
+    if mask is None:
+        return None
+    if mask.dtype == torch.bool:
+        mask = mask.view(torch.uint8)
+    if mask.dtype != torch.uint8 or not mask.is_contiguous():
+        raise SdpaError(5)
+    return mask.data_ptr()
+
+
+class SdpaPlan:
+    """A validated, pre-encoded forward (sdpa_plan_create): ``launch()`` only
+    enqueues the kernel.  Bound to the shapes, strides, dtype, mask mode and
+    scale given here; ``set_pointers`` moves it to other tensors of the same
+    layout.  Keep the tensors alive while launches are in flight."""
+
+    def __init__(self, q, k, v, out, *, is_causal=False, mask=None, scale=None):
+        lib = load_library()
+        handle = ctypes.c_void_p(None)
+        s = float("nan") if scale is None else float(scale)
+        rc = lib.sdpa_plan_create(
+            ctypes.byref(handle), ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k.data_ptr()),
+            ctypes.c_void_p(v.data_ptr()), ctypes.c_void_p(out.data_ptr()), _dtype_code(q),
+            q.dim(), _arr(q.shape), _arr(q.stride()), _arr(k.stride()), _arr(v.stride()),
+            _arr(out.stride()), 1 if is_causal else 0,
+            ctypes.c_void_p(_mask_ptr(mask)) if mask is not None else None, ctypes.c_float(s))
+        if rc != 0:
+            raise SdpaError(rc, "sdpa_plan_create")
+        self._lib, self._h = lib, handle
+
+    def set_pointers(self, q, k, v, out, mask=None):
+        mp = _mask_ptr(mask)
+        rc = self._lib.sdpa_plan_set_pointers(
+            self._h, ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k.data_ptr()),
+            ctypes.c_void_p(v.data_ptr()), ctypes.c_void_p(out.data_ptr()),
+            ctypes.c_void_p(mp) if mp else None)
+        if rc != 0:
+            raise SdpaError(rc, "sdpa_plan_set_pointers")
+
+    def launch(self, stream=None):
+        import torch
+        st = (stream if stream is not None else torch.cuda.current_stream()).cuda_stream
+        rc = self._lib.sdpa_plan_launch(self._h, ctypes.c_void_p(st) if st else None)
+        if rc != 0:
+            raise SdpaError(rc, "sdpa_plan_launch")
+
+    def close(self):
+        if getattr(self, "_h", None) is not None and self._h.value:
+            self._lib.sdpa_plan_destroy(self._h)
+            self._h = ctypes.c_void_p(None)
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:  # pragma: no cover - interpreter shutdown
+            pass
 
 
 def sdpa_last_device_status(stream=None):

@@ -57,6 +57,17 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
   return t;
 }
 
+// Programmatic dependent launch: wait until the grids this launch depends
+// on have completed and their memory is visible (a no-op when the launch
+// has no programmatic dependency), and let the next grid in the stream be
+// scheduled early (it still waits for this grid's completion itself).
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // true in exactly one lane of the (fully active) warp.
 __device__ __forceinline__ bool elect_one() {
   uint32_t pred;

@@ -16,6 +16,7 @@
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <new>
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -198,30 +199,38 @@ sdpa_status validate(const void* q, const void* k, const void* v, void* out, sdp
   return SDPA_OK;
 }
 
-}  // namespace
 
-extern "C" {
-
-sdpa_status sdpa_forward(const void* q, const void* k, const void* v, void* out,
-                         sdpa_dtype dtype, int rank, const int64_t* shape,
-                         const int64_t* q_stride, const int64_t* k_stride,
-                         const int64_t* v_stride, const int64_t* o_stride, int is_causal,
-                         const uint8_t* mask, float scale, void* stream) {
+// Everything a launch needs, built once from validated arguments.
+struct Prepared {
+  sdpa_impl::FwdParams p;
   View views[4];
+  int mode;
+  int head_dim;
+  bool bf16;
+  int device;
+};
+
+sdpa_status build_params(const void* q, const void* k, const void* v, void* out, sdpa_dtype dtype,
+                         int rank, const int64_t* shape, const int64_t* q_stride,
+                         const int64_t* k_stride, const int64_t* v_stride,
+                         const int64_t* o_stride, int is_causal, const uint8_t* mask, float scale,
+                         Prepared* pr) {
   sdpa_status s = validate(q, k, v, out, dtype, rank, shape, q_stride, k_stride, v_stride,
-                           o_stride, is_causal, mask, scale, views);
+                           o_stride, is_causal, mask, scale, pr->views);
   if (s != SDPA_OK) return s;
   s = check_device();
   if (s != SDPA_OK) return s;
+  if (cudaGetDevice(&pr->device) != cudaSuccess) return SDPA_ERR_CUDA;
 
-  const bool bf16 = (dtype == SDPA_BF16);
+  pr->bf16 = (dtype == SDPA_BF16);
+  const View* views = pr->views;
   const int64_t B = views[0].ext[0], H = views[0].ext[1], L = views[0].ext[2],
                 D = views[0].ext[3];
-  sdpa_impl::FwdParams p;
+  sdpa_impl::FwdParams& p = pr->p;
   std::memset(&p, 0, sizeof(p));
-  if ((s = encode_map(views[0], bf16, &p.tm_q, p.pos_q)) != SDPA_OK) return s;
-  if ((s = encode_map(views[1], bf16, &p.tm_k, p.pos_k)) != SDPA_OK) return s;
-  if ((s = encode_map(views[2], bf16, &p.tm_v, p.pos_v)) != SDPA_OK) return s;
+  if ((s = encode_map(views[0], pr->bf16, &p.tm_q, p.pos_q)) != SDPA_OK) return s;
+  if ((s = encode_map(views[1], pr->bf16, &p.tm_k, p.pos_k)) != SDPA_OK) return s;
+  if ((s = encode_map(views[2], pr->bf16, &p.tm_v, p.pos_v)) != SDPA_OK) return s;
   p.out = out;
   p.o_sb = views[3].str[0];
   p.o_sh = views[3].str[1];
@@ -240,15 +249,125 @@ sdpa_status sdpa_forward(const void* q, const void* k, const void* v, void* out,
   // times it rounds the exponent to 0 and the weights are exactly 1.0f.
   if (p.scale_log2 == 0.0f) p.scale_log2 = std::signbit(sc) ? -FLT_MIN : FLT_MIN;
   p.mask_vec16 = (mask && (L % 16) == 0 && (reinterpret_cast<uintptr_t>(mask) & 15u) == 0);
+  pr->mode = is_causal ? sdpa_impl::kMaskCausal
+                       : (mask ? sdpa_impl::kMaskExplicit : sdpa_impl::kMaskNone);
+  pr->head_dim = static_cast<int>(D);
+  return SDPA_OK;
+}
+
+sdpa_status launch_prepared(const Prepared& pr, void* stream) {
+  sdpa_impl::FwdParams p = pr.p;
   p.debug_withhold_q = g_withhold_q.load(std::memory_order_relaxed);
   p.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
-
-  const int mode = is_causal ? sdpa_impl::kMaskCausal
-                             : (mask ? sdpa_impl::kMaskExplicit : sdpa_impl::kMaskNone);
-  const cudaError_t e = sdpa_impl::launch_forward(p, static_cast<int>(D), mode, bf16,
+  const cudaError_t e = sdpa_impl::launch_forward(p, pr.head_dim, pr.mode, pr.bf16,
                                                   static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;
 }
+
+using ReplaceAddressFn = CUresult (*)(CUtensorMap*, void*);
+
+ReplaceAddressFn get_replace_fn() {
+  static std::once_flag once;
+  static ReplaceAddressFn fn = nullptr;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapReplaceAddress", &ptr, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<ReplaceAddressFn>(ptr);
+  });
+  return fn;
+}
+
+}  // namespace
+
+struct sdpa_plan {
+  Prepared pr;
+  int64_t shape[4];
+  int64_t strides[4][4];
+  int rank;
+  int is_causal;
+  float scale;
+  sdpa_dtype dtype;
+};
+
+extern "C" {
+
+sdpa_status sdpa_forward(const void* q, const void* k, const void* v, void* out,
+                         sdpa_dtype dtype, int rank, const int64_t* shape,
+                         const int64_t* q_stride, const int64_t* k_stride,
+                         const int64_t* v_stride, const int64_t* o_stride, int is_causal,
+                         const uint8_t* mask, float scale, void* stream) {
+  Prepared pr;
+  const sdpa_status s = build_params(q, k, v, out, dtype, rank, shape, q_stride, k_stride,
+                                     v_stride, o_stride, is_causal, mask, scale, &pr);
+  if (s != SDPA_OK) return s;
+  return launch_prepared(pr, stream);
+}
+
+sdpa_status sdpa_plan_create(sdpa_plan** plan, const void* q, const void* k, const void* v,
+                             void* out, sdpa_dtype dtype, int rank, const int64_t* shape,
+                             const int64_t* q_stride, const int64_t* k_stride,
+                             const int64_t* v_stride, const int64_t* o_stride, int is_causal,
+                             const uint8_t* mask, float scale) {
+  if (!plan) return SDPA_ERR_NULL;
+  *plan = nullptr;
+  sdpa_plan* pl = new (std::nothrow) sdpa_plan;
+  if (!pl) return SDPA_ERR_ARG;
+  const sdpa_status s = build_params(q, k, v, out, dtype, rank, shape, q_stride, k_stride,
+                                     v_stride, o_stride, is_causal, mask, scale, &pl->pr);
+  if (s != SDPA_OK) {
+    delete pl;
+    return s;
+  }
+  pl->rank = rank;
+  pl->is_causal = is_causal;
+  pl->scale = scale;
+  pl->dtype = dtype;
+  const int64_t* st[4] = {q_stride, k_stride, v_stride, o_stride};
+  for (int i = 0; i < rank; ++i) {
+    pl->shape[i] = shape[i];
+    for (int t = 0; t < 4; ++t) pl->strides[t][i] = st[t][i];
+  }
+  *plan = pl;
+  return SDPA_OK;
+}
+
+sdpa_status sdpa_plan_set_pointers(sdpa_plan* plan, const void* q, const void* k, const void* v,
+                                   void* out, const uint8_t* mask) {
+  if (!plan) return SDPA_ERR_NULL;
+  if ((plan->pr.p.mask != nullptr) != (mask != nullptr)) return SDPA_ERR_ARG;
+  // Full validation of the new addresses against the plan's shape and strides.
+  View views[4];
+  sdpa_status s = validate(q, k, v, out, plan->dtype, plan->rank, plan->shape, plan->strides[0],
+                           plan->strides[1], plan->strides[2], plan->strides[3],
+                           plan->is_causal, mask, plan->scale, views);
+  if (s != SDPA_OK) return s;
+  ReplaceAddressFn rep = get_replace_fn();
+  if (!rep) return SDPA_ERR_CUDA;
+  sdpa_impl::FwdParams p = plan->pr.p;
+  if (rep(&p.tm_q, const_cast<void*>(q)) != CUDA_SUCCESS ||
+      rep(&p.tm_k, const_cast<void*>(k)) != CUDA_SUCCESS ||
+      rep(&p.tm_v, const_cast<void*>(v)) != CUDA_SUCCESS)
+    return SDPA_ERR_LAYOUT;
+  p.out = out;
+  p.mask = mask;
+  p.mask_vec16 = (mask && (p.L % 16) == 0 && (reinterpret_cast<uintptr_t>(mask) & 15u) == 0);
+  plan->pr.p = p;
+  for (int t = 0; t < 4; ++t) plan->pr.views[t] = views[t];
+  return SDPA_OK;
+}
+
+sdpa_status sdpa_plan_launch(const sdpa_plan* plan, void* stream) {
+  if (!plan) return SDPA_ERR_NULL;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SDPA_ERR_CUDA;
+  if (dev != plan->pr.device) return SDPA_ERR_ARG;
+  return launch_prepared(plan->pr, stream);
+}
+
+void sdpa_plan_destroy(sdpa_plan* plan) { delete plan; }
 
 const char* sdpa_status_string(sdpa_status status) {
   switch (status) {

@@ -497,6 +497,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // Everything above (barrier set-up, TMEM allocation, descriptor prefetch)
+  // may overlap the previous kernel in the stream; nothing below touches
+  // global memory before that kernel has completed.
+  grid_dependency_wait();
+  grid_launch_dependents();
   const uint32_t tmem = bars->tmem_base;
   // TMEM columns: S_A [0,128), S_B [128,256), O_A [256, 256+D), O_B [256+D, 256+2D),
   // and with D = 64 also P_A [384, 448), P_B [448, 512).
@@ -728,9 +733,20 @@ cudaError_t launch_one(const sdpa_impl::FwdParams& p, cudaStream_t stream) {
     configured = true;
   }
   const unsigned pairs = static_cast<unsigned>((p.n_tiles + 1) / 2);
-  dim3 grid(pairs * static_cast<unsigned>(p.B * p.H));
-  kern<<<grid, kThreads, smem, stream>>>(p);
-  return cudaGetLastError();
+  // Programmatic dependent launch: this grid's set-up may start while the
+  // previous kernel in the stream drains; the kernel waits for it
+  // (griddepcontrol.wait) before its first global-memory access.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(pairs * static_cast<unsigned>(p.B * p.H));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
 template <int D, bool BF16>
