@@ -64,11 +64,11 @@ def load_variant(lib_path: str):
 def _bind(lib):
     d, i64, u8p = ctypes.POINTER(ctypes.c_double), ctypes.c_int64, ctypes.c_void_p
     lib.oracle_sdpa_fp64.argtypes = [d, d, d, d, i64, i64, i64, i64, u8p,
-                                     ctypes.c_int, ctypes.c_double]
+                                     ctypes.c_int, ctypes.c_double, d]
     lib.oracle_sdpa_fp64.restype = ctypes.c_int
     lib.oracle_sdpa_rows_fp64.argtypes = [d, d, d, i64, i64, i64, i64, u8p,
                                           ctypes.c_int, ctypes.c_double,
-                                          ctypes.POINTER(ctypes.c_int64), i64, d]
+                                          ctypes.POINTER(ctypes.c_int64), i64, d, d]
     lib.oracle_sdpa_rows_fp64.restype = ctypes.c_int
     lib.oracle_num_threads.argtypes = []
     lib.oracle_num_threads.restype = ctypes.c_int
@@ -128,11 +128,13 @@ def default_scale(D: int) -> float:
     return 1.0 / math.sqrt(D)
 
 
-def sdpa(q, k, v, mask=None, is_causal=False, scale=None, _lib_override=None) -> np.ndarray:
+def sdpa(q, k, v, mask=None, is_causal=False, scale=None, _lib_override=None,
+         return_lse=False):
     """Full attention output in fp64, same rank as ``q`` ([H,L,D] or [B,H,L,D]).
 
     ``mask``: optional [L, L], nonzero = removed (masked_fill polarity).
-    ``scale``: None -> 1/sqrt(D)."""
+    ``scale``: None -> 1/sqrt(D).  ``return_lse``: also return the per-row
+    log-sum-exp of the scaled, masked scores (shape of ``q`` without D)."""
     q, k, v = _as_f64(q), _as_f64(k), _as_f64(v)
     if not (q.shape == k.shape == v.shape):
         raise ValueError("q, k, v must share one shape")
@@ -140,34 +142,38 @@ def sdpa(q, k, v, mask=None, is_causal=False, scale=None, _lib_override=None) ->
     m = _as_mask(mask, L)
     s = default_scale(D) if scale is None else float(scale)
     out = np.empty_like(q)
+    lse = np.empty(q.shape[:-1], dtype=np.float64) if return_lse else None
     dp = ctypes.POINTER(ctypes.c_double)
     lib = _lib_override if _lib_override is not None else _load()
     rc = lib.oracle_sdpa_fp64(
         q.ctypes.data_as(dp), k.ctypes.data_as(dp), v.ctypes.data_as(dp),
         out.ctypes.data_as(dp), B, H, L, D,
-        None if m is None else m.ctypes.data, int(bool(is_causal)), s)
+        None if m is None else m.ctypes.data, int(bool(is_causal)), s,
+        None if lse is None else lse.ctypes.data_as(dp))
     if rc != 0:
         raise RuntimeError("oracle_sdpa_fp64 failed")
-    return out
+    return (out, lse) if return_lse else out
 
 
 def sdpa_rows(q, k, v, rows, mask=None, is_causal=False, scale=None,
-              _lib_override=None) -> np.ndarray:
+              _lib_override=None, return_lse=False):
     """Output rows for the (b, h, i) triples in ``rows`` (shape [n, 3]); for
-    rank-3 inputs pass b = 0.  Returns [n, D] fp64."""
+    rank-3 inputs pass b = 0.  Returns [n, D] fp64 (and [n] log-sum-exp
+    values with ``return_lse``)."""
     q, k, v = _as_f64(q), _as_f64(k), _as_f64(v)
     B, H, L, D = _shape4(q)
     m = _as_mask(mask, L)
     idx = np.ascontiguousarray(np.asarray(rows, dtype=np.int64).reshape(-1, 3))
     s = default_scale(D) if scale is None else float(scale)
     out = np.empty((idx.shape[0], D), dtype=np.float64)
+    lse = np.empty(idx.shape[0], dtype=np.float64) if return_lse else None
     dp = ctypes.POINTER(ctypes.c_double)
     lib = _lib_override if _lib_override is not None else _load()
     rc = lib.oracle_sdpa_rows_fp64(
         q.ctypes.data_as(dp), k.ctypes.data_as(dp), v.ctypes.data_as(dp),
         B, H, L, D, None if m is None else m.ctypes.data, int(bool(is_causal)), s,
         idx.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), idx.shape[0],
-        out.ctypes.data_as(dp))
+        out.ctypes.data_as(dp), None if lse is None else lse.ctypes.data_as(dp))
     if rc != 0:
         raise RuntimeError("oracle_sdpa_rows_fp64 failed (row index out of range?)")
-    return out
+    return (out, lse) if return_lse else out

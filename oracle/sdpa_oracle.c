@@ -37,6 +37,10 @@
  *
  * Layout: q, k, v, out are dense row-major [B, H, L, D] doubles; mask, when
  * not NULL, is a dense row-major [L, L] byte matrix shared by every (b, h).
+ * lse, when not NULL, receives per row the log-sum-exp of the scaled,
+ * masked scores (the log of the softmax denominator; -inf for a row with no
+ * admissible key) -- the second output of the fused forward that the
+ * FlashInfer pull-request page shows as `out, lse = fwd(...)`.
  */
 #include <math.h>
 #include <stdint.h>
@@ -51,7 +55,7 @@
 static void attend_one_row(const double *qi, const double *K, const double *V,
                            int64_t L, int64_t D, int64_t i,
                            const uint8_t *mask_row, int is_causal, double scale,
-                           double *s, double *out_row)
+                           double *s, double *out_row, double *lse)
 {
     int64_t j, d;
 
@@ -88,6 +92,8 @@ static void attend_one_row(const double *qi, const double *K, const double *V,
         /* every key removed: the safe softmax gives a zero row */
         for (j = 0; j < L; ++j)
             s[j] = 0.0;
+        if (lse)
+            *lse = -INFINITY; /* log of an empty sum */
     } else {
         double total = 0.0;
         for (j = 0; j < L; ++j) {
@@ -96,6 +102,10 @@ static void attend_one_row(const double *qi, const double *K, const double *V,
         }
         for (j = 0; j < L; ++j)
             s[j] = s[j] / total;
+        /* log-sum-exp of the scaled, masked scores: the softmax denominator
+         * in log form, log(sum_j exp(s_j)) = m + log(sum_j exp(s_j - m)) */
+        if (lse)
+            *lse = m + log(total);
     }
 
     /* step 5: out_i = attn_i . V */
@@ -113,7 +123,8 @@ static void attend_one_row(const double *qi, const double *K, const double *V,
  * argument or an allocation failure. */
 int oracle_sdpa_fp64(const double *q, const double *k, const double *v,
                      double *out, int64_t B, int64_t H, int64_t L, int64_t D,
-                     const uint8_t *mask, int is_causal, double scale)
+                     const uint8_t *mask, int is_causal, double scale,
+                     double *lse)
 {
     if (!q || !k || !v || !out || B < 0 || H < 0 || L < 0 || D < 1)
         return -1;
@@ -135,7 +146,7 @@ int oracle_sdpa_fp64(const double *q, const double *k, const double *v,
                              *V = v + bh * L * D;
                 attend_one_row(Q + i * D, K, V, L, D, i,
                                mask ? mask + i * L : NULL, is_causal, scale, s,
-                               out + r * D);
+                               out + r * D, lse ? lse + r : NULL);
             }
             free(s);
         }
@@ -148,7 +159,8 @@ int oracle_sdpa_fp64(const double *q, const double *k, const double *v,
 int oracle_sdpa_rows_fp64(const double *q, const double *k, const double *v,
                           int64_t B, int64_t H, int64_t L, int64_t D,
                           const uint8_t *mask, int is_causal, double scale,
-                          const int64_t *idx, int64_t n, double *out_rows)
+                          const int64_t *idx, int64_t n, double *out_rows,
+                          double *lse_rows)
 {
     if (!q || !k || !v || !idx || !out_rows || L < 1 || D < 1)
         return -1;
@@ -175,7 +187,7 @@ int oracle_sdpa_rows_fp64(const double *q, const double *k, const double *v,
                 attend_one_row(q + (bh * L + i) * D, k + bh * L * D,
                                v + bh * L * D, L, D, i,
                                mask ? mask + i * L : NULL, is_causal, scale, s,
-                               out_rows + t * D);
+                               out_rows + t * D, lse_rows ? lse_rows + t : NULL);
             }
             free(s);
         }

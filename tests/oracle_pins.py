@@ -19,7 +19,11 @@ Sources of truth used here:
     one vector c (each row's scores move by the constant q.c);
   * torch's CPU math backend in fp64, the backend that page calls the correct,
     NaN-safe reference (its boolean attn_mask means True = attend, so the mask
-    is inverted for it).
+    is inverted for it);
+  * for the log-sum-exp output (the log of the softmax denominator): decimal
+    brute force, closed forms (q = 0 -> log of the number of admissible keys,
+    one admissible key -> its scaled score, no admissible key -> -inf) and
+    torch.logsumexp over explicitly computed, masked scores.
 """
 from __future__ import annotations
 
@@ -205,11 +209,87 @@ def pin_torch_math_backend(impl):
                                    rtol=0, atol=1e-12)
 
 
+def _lse_impl(impl):
+    """The pins call impl(q, k, v, ...); LSE pins need its second output."""
+    def f(q, k, v, **kw):
+        return impl(q, k, v, return_lse=True, **kw)[1]
+    return f
+
+
+def brute_force_lse_decimal(q, k, mask=None, is_causal=False, scale=None):
+    getcontext().prec = 40
+    H, L, D = q.shape
+    sc = Decimal(float(1.0 / np.sqrt(D) if scale is None else scale))
+    out = np.zeros((H, L))
+    for h in range(H):
+        for i in range(L):
+            keys = [j for j in range(L)
+                    if not (is_causal and j > i) and not (mask is not None and mask[i, j])]
+            if not keys:
+                out[h, i] = -np.inf
+                continue
+            z = sum((sum(Decimal(float(q[h, i, d])) * Decimal(float(k[h, j, d]))
+                         for d in range(D)) * sc).exp() for j in keys)
+            out[h, i] = float(z.ln())
+    return out
+
+
+def pin_lse_brute_force(impl):
+    lse = _lse_impl(impl)
+    for (q, k, v, mask, causal, scale) in _tiny_cases():
+        got = lse(q, k, v, mask=mask, is_causal=causal, scale=scale)
+        ref = brute_force_lse_decimal(q, k, mask, causal, scale)
+        fin = np.isfinite(ref)
+        assert np.array_equal(np.isfinite(got), fin)
+        assert np.all(got[~fin] == -np.inf)
+        np.testing.assert_allclose(got[fin], ref[fin], rtol=0, atol=1e-13)
+
+
+def pin_lse_closed_forms(impl):
+    lse = _lse_impl(impl)
+    g = _rng(22)
+    H, L, D = 2, 7, 4
+    # q = 0: every admissible score is 0, so the sum has (#keys) ones
+    q0, k, v = np.zeros((H, L, D)), g.standard_normal((H, L, D)), g.standard_normal((H, L, D))
+    np.testing.assert_allclose(lse(q0, k, v, is_causal=True),
+                               np.broadcast_to(np.log(np.arange(1, L + 1)), (H, L)),
+                               rtol=0, atol=1e-14)
+    # one admissible key j: the sum is the single term exp(scale * q_i . k_j)
+    q = g.standard_normal((H, L, D))
+    perm = g.permutation(L)
+    mask = np.ones((L, L), dtype=bool)
+    mask[np.arange(L), perm] = False
+    expect = 0.5 * np.einsum("hid,hid->hi", q, k[:, perm, :])
+    np.testing.assert_allclose(lse(q, k, v, mask=mask, scale=0.5), expect, rtol=0, atol=1e-14)
+    # a fully removed row has an empty sum: -inf
+    mask2 = np.zeros((L, L), dtype=bool)
+    mask2[3] = True
+    got = lse(q, k, v, mask=mask2)
+    assert got[0, 3] == -np.inf and got[1, 3] == -np.inf
+    assert np.all(np.isfinite(np.delete(got, 3, axis=1)))
+
+
+def pin_lse_torch_logsumexp(impl):
+    import torch
+    lse = _lse_impl(impl)
+    g = _rng(23)
+    B, H, L, D = 2, 3, 19, 8
+    q, k, v = (g.standard_normal((B, H, L, D)) for _ in range(3))
+    mask = g.random((L, L)) < 0.3
+    mask[:, 0] = False
+    scores = torch.from_numpy(q) @ torch.from_numpy(k).transpose(-1, -2) * 0.7
+    scores = scores.masked_fill(torch.from_numpy(mask), float("-inf"))
+    np.testing.assert_allclose(lse(q, k, v, mask=mask, scale=0.7),
+                               torch.logsumexp(scores, dim=-1).numpy(), rtol=0, atol=1e-12)
+
+
 ALL_PINS = [pin_brute_force, pin_causal_row0, pin_zero_query_prefix_mean, pin_zero_scale_mean,
             pin_single_key, pin_equal_keys, pin_fully_masked_rows_zero, pin_weights_sum_to_one,
             pin_linearity_in_v, pin_permutation_invariance, pin_key_shift_invariance,
-            pin_torch_math_backend]
+            pin_torch_math_backend, pin_lse_brute_force, pin_lse_closed_forms,
+            pin_lse_torch_logsumexp]
 
 # Pins that do not lean on a library: the mutation test requires that each
 # planted mistake is caught by at least one of these alone.
-INDEPENDENT_PINS = [p for p in ALL_PINS if p is not pin_torch_math_backend]
+INDEPENDENT_PINS = [p for p in ALL_PINS
+                    if p not in (pin_torch_math_backend, pin_lse_torch_logsumexp)]

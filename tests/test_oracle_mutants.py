@@ -25,6 +25,8 @@ MUTANTS = {
     "unsafe_softmax": ("if (m == -INFINITY) {", "if (0) {"),
     "v_wrong_row": ("const double *vj = V + j * D;", "const double *vj = V + i * D;"),
     "wrong_normaliser": ("total += s[j];", "total += s[j] * s[j];"),
+    "lse_without_max": ("*lse = m + log(total);", "*lse = log(total);"),
+    "lse_of_empty_row_zero": ("*lse = -INFINITY; /* log of an empty sum */", "*lse = 0.0;"),
     "mask_row_of_query_0": ("mask ? mask + i * L : NULL, is_causal, scale, s,\n                               out + r * D",
                             "mask ? mask : NULL, is_causal, scale, s,\n                               out + r * D"),
 }
