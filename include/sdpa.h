@@ -147,6 +147,34 @@ SDPA_API sdpa_status sdpa_plan_set_pointers(sdpa_plan* plan, const void* q, cons
 SDPA_API sdpa_status sdpa_plan_launch(const sdpa_plan* plan, void* stream);
 SDPA_API void sdpa_plan_destroy(sdpa_plan* plan);
 
+/*
+ * sdpa_forward_lse -- sdpa_forward that also writes, per query row, the
+ * log-sum-exp of the scaled, masked scores, log(sum_j exp(scale * q_i . k_j))
+ * over the admissible keys (-inf for a row with none): the log of the
+ * softmax denominator, the second output of the fused forward on the
+ * FlashInfer pull-request page (`out, lse = fwd(...)`), which a backward
+ * pass or a merge of partial results needs.
+ *
+ * lse        : DEVICE float32 buffer of shape [B, H, L] (rank 4) or [H, L]
+ *              (rank 3), 4-byte aligned, not overlapping any other operand.
+ * lse_stride : rank - 1 strides in ELEMENTS (host array); positive unless
+ *              the extent is 1.
+ * Everything else as sdpa_forward; SDPA_ERR_NULL if lse or lse_stride is
+ * NULL.  The LSE is computed in fp32 from the same running maximum and sum
+ * the softmax uses.
+ */
+SDPA_API sdpa_status sdpa_forward_lse(const void* q, const void* k, const void* v, void* out,
+                                      float* lse, sdpa_dtype dtype, int rank,
+                                      const int64_t* shape, const int64_t* q_stride,
+                                      const int64_t* k_stride, const int64_t* v_stride,
+                                      const int64_t* o_stride, const int64_t* lse_stride,
+                                      int is_causal, const uint8_t* mask, float scale,
+                                      void* stream);
+
+/* Adds (lse != NULL) or removes (lse == NULL) the log-sum-exp output of a
+ * plan; same layout rules as sdpa_forward_lse. */
+SDPA_API sdpa_status sdpa_plan_set_lse(sdpa_plan* plan, float* lse, const int64_t* lse_stride);
+
 /* Human-readable name of a status code (static storage, never NULL). */
 SDPA_API const char* sdpa_status_string(sdpa_status status);
 

@@ -78,6 +78,12 @@ def load_library(path: str | None = None):
     lib.sdpa_plan_launch.restype = ctypes.c_int
     lib.sdpa_plan_destroy.argtypes = [vp]
     lib.sdpa_plan_destroy.restype = None
+    lib.sdpa_forward_lse.argtypes = [vp, vp, vp, vp, vp, ctypes.c_int, ctypes.c_int, i64p,
+                                     i64p, i64p, i64p, i64p, i64p, ctypes.c_int, vp,
+                                     ctypes.c_float, vp]
+    lib.sdpa_forward_lse.restype = ctypes.c_int
+    lib.sdpa_plan_set_lse.argtypes = [vp, vp, i64p]
+    lib.sdpa_plan_set_lse.restype = ctypes.c_int
     if path is None:
         _lib = lib
     return lib
@@ -132,14 +138,16 @@ def sdpa_forward_raw(q_ptr: int, k_ptr: int, v_ptr: int, out_ptr: int, dtype: in
 
 
 def sdpa_forward(q, k, v, out=None, *, is_causal: bool = False, mask=None, scale=None,
-                 stream=None):
+                 stream=None, return_lse: bool = False, lse=None):
     """Fused attention forward on torch CUDA tensors.
 
     q, k, v: [H, L, D] or [B, H, L, D], bf16 or fp16, any strides with the
     last one 1.  mask: optional [L, L] bool/uint8 on the same device (True /
     nonzero = removed).  scale: None -> 1/sqrt(D).  out: optional
     preallocated output (may be a strided view).  Launches on ``stream`` (a
-    torch.cuda.Stream) or the current stream; returns ``out``.
+    torch.cuda.Stream) or the current stream; returns ``out``, or
+    ``(out, lse)`` with ``return_lse`` (lse: fp32, q's shape without D; an
+    existing buffer may be passed as ``lse``).
     """
     import torch
 
@@ -166,12 +174,27 @@ def sdpa_forward(q, k, v, out=None, *, is_causal: bool = False, mask=None, scale
         mptr = mask.data_ptr()
     s = float("nan") if scale is None else float(scale)
     st = (stream if stream is not None else torch.cuda.current_stream(q.device)).cuda_stream
-    rc = sdpa_forward_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), dt, q.dim(),
-                          list(q.shape), q.stride(), k.stride(), v.stride(), out.stride(),
-                          is_causal, mptr, s, st)
+    if not (return_lse or lse is not None):
+        rc = sdpa_forward_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), dt,
+                              q.dim(), list(q.shape), q.stride(), k.stride(), v.stride(),
+                              out.stride(), is_causal, mptr, s, st)
+        if rc != 0:
+            raise SdpaError(rc)
+        return out
+    if lse is None:
+        lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
+    elif lse.dtype != torch.float32 or tuple(lse.shape) != tuple(q.shape[:-1]):
+        raise SdpaError(3)
+    rc = load_library().sdpa_forward_lse(
+        ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k.data_ptr()),
+        ctypes.c_void_p(v.data_ptr()), ctypes.c_void_p(out.data_ptr()),
+        ctypes.c_void_p(lse.data_ptr()), dt, q.dim(), _arr(q.shape), _arr(q.stride()),
+        _arr(k.stride()), _arr(v.stride()), _arr(out.stride()), _arr(lse.stride()),
+        1 if is_causal else 0, ctypes.c_void_p(mptr) if mptr else None, ctypes.c_float(s),
+        ctypes.c_void_p(st) if st else None)
     if rc != 0:
-        raise SdpaError(rc)
-    return out
+        raise SdpaError(rc, "sdpa_forward_lse")
+    return out, lse
 
 
 def _dtype_code(q):
@@ -222,6 +245,17 @@ class SdpaPlan:
             ctypes.c_void_p(mp) if mp else None)
         if rc != 0:
             raise SdpaError(rc, "sdpa_plan_set_pointers")
+
+    def set_lse(self, lse=None):
+        """Also write the per-row log-sum-exp into ``lse`` (fp32, q's shape
+        without D) on every launch; None removes it."""
+        if lse is None:
+            rc = self._lib.sdpa_plan_set_lse(self._h, None, None)
+        else:
+            rc = self._lib.sdpa_plan_set_lse(self._h, ctypes.c_void_p(lse.data_ptr()),
+                                             _arr(lse.stride()))
+        if rc != 0:
+            raise SdpaError(rc, "sdpa_plan_set_lse")
 
     def launch(self, stream=None):
         import torch

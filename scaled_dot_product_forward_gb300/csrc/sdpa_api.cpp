@@ -200,6 +200,36 @@ sdpa_status validate(const void* q, const void* k, const void* v, void* out, sdp
 }
 
 
+// Optional log-sum-exp output: fp32, rank - 1 extents (the shape without D),
+// element strides, 4-byte aligned, not overlapping any other operand.
+sdpa_status check_lse(const float* lse, int rank, const int64_t* shape, const int64_t* stride,
+                      const View views[4], const uint8_t* mask, int64_t out_stride[3]) {
+  if (!stride) return SDPA_ERR_NULL;
+  if ((reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return SDPA_ERR_LAYOUT;
+  const int off = 4 - rank;  // rank 3: batch extent 1
+  uint64_t last = 0;
+  for (int i = 0; i < 3; ++i) {
+    const int64_t ext = (i < off) ? 1 : shape[i - off];
+    const int64_t st = (i < off) ? 0 : stride[i - off];
+    if (ext > 1 && st <= 0) return SDPA_ERR_LAYOUT;
+    out_stride[i] = (ext > 1) ? st : 0;
+    last += static_cast<uint64_t>(ext - 1) * static_cast<uint64_t>(out_stride[i]);
+  }
+  const uintptr_t l0 = reinterpret_cast<uintptr_t>(lse), l1 = l0 + 4 * (last + 1);
+  for (int t = 0; t < 4; ++t) {
+    uintptr_t a0, a1;
+    span_of(views[t], &a0, &a1);
+    if (overlaps(l0, l1, a0, a1)) return SDPA_ERR_ARG;
+  }
+  if (mask) {
+    const int64_t L = views[0].ext[2];
+    const uintptr_t m0 = reinterpret_cast<uintptr_t>(mask);
+    if (overlaps(l0, l1, m0, m0 + static_cast<uintptr_t>(L) * static_cast<uintptr_t>(L)))
+      return SDPA_ERR_ARG;
+  }
+  return SDPA_OK;
+}
+
 // Everything a launch needs, built once from validated arguments.
 struct Prepared {
   sdpa_impl::FwdParams p;
@@ -306,6 +336,29 @@ sdpa_status sdpa_forward(const void* q, const void* k, const void* v, void* out,
   return launch_prepared(pr, stream);
 }
 
+sdpa_status sdpa_forward_lse(const void* q, const void* k, const void* v, void* out, float* lse,
+                             sdpa_dtype dtype, int rank, const int64_t* shape,
+                             const int64_t* q_stride, const int64_t* k_stride,
+                             const int64_t* v_stride, const int64_t* o_stride,
+                             const int64_t* lse_stride, int is_causal, const uint8_t* mask,
+                             float scale, void* stream) {
+  if (!lse) return SDPA_ERR_NULL;
+  Prepared pr;
+  sdpa_status s = validate(q, k, v, out, dtype, rank, shape, q_stride, k_stride, v_stride,
+                           o_stride, is_causal, mask, scale, pr.views);
+  if (s != SDPA_OK) return s;
+  int64_t ls[3];
+  if ((s = check_lse(lse, rank, shape, lse_stride, pr.views, mask, ls)) != SDPA_OK) return s;
+  s = build_params(q, k, v, out, dtype, rank, shape, q_stride, k_stride, v_stride, o_stride,
+                   is_causal, mask, scale, &pr);
+  if (s != SDPA_OK) return s;
+  pr.p.lse = lse;
+  pr.p.lse_sb = ls[0];
+  pr.p.lse_sh = ls[1];
+  pr.p.lse_sl = ls[2];
+  return launch_prepared(pr, stream);
+}
+
 sdpa_status sdpa_plan_create(sdpa_plan** plan, const void* q, const void* k, const void* v,
                              void* out, sdpa_dtype dtype, int rank, const int64_t* shape,
                              const int64_t* q_stride, const int64_t* k_stride,
@@ -365,6 +418,23 @@ sdpa_status sdpa_plan_launch(const sdpa_plan* plan, void* stream) {
   if (cudaGetDevice(&dev) != cudaSuccess) return SDPA_ERR_CUDA;
   if (dev != plan->pr.device) return SDPA_ERR_ARG;
   return launch_prepared(plan->pr, stream);
+}
+
+sdpa_status sdpa_plan_set_lse(sdpa_plan* plan, float* lse, const int64_t* lse_stride) {
+  if (!plan) return SDPA_ERR_NULL;
+  if (!lse) {
+    plan->pr.p.lse = nullptr;
+    return SDPA_OK;
+  }
+  int64_t ls[3];
+  const sdpa_status s = check_lse(lse, plan->rank, plan->shape, lse_stride, plan->pr.views,
+                                  plan->pr.p.mask, ls);
+  if (s != SDPA_OK) return s;
+  plan->pr.p.lse = lse;
+  plan->pr.p.lse_sb = ls[0];
+  plan->pr.p.lse_sh = ls[1];
+  plan->pr.p.lse_sl = ls[2];
+  return SDPA_OK;
 }
 
 void sdpa_plan_destroy(sdpa_plan* plan) { delete plan; }

@@ -424,6 +424,12 @@ __device__ __forceinline__ void softmax_role(const sdpa_impl::FwdParams& p, cons
   if (ok && warp_wait_phase(&bars->o_done[t], (n - 1) & 1, bars, limit, kSiteODone)) {
     tc_fence_after();
     const float inv_l = (l > 0.0f) ? (1.0f / l) : 0.0f;
+    if (p.lse != nullptr && row_g < p.L) {
+      // log(sum_j exp(scale * s_j)) = ln(l) + m_used * ln(2): l sums 2^(x - m_used).
+      constexpr float kLn2 = 0.693147180559945309f;
+      p.lse[w.batch * p.lse_sb + w.head * p.lse_sh + static_cast<int64_t>(row_g) * p.lse_sl] =
+          (l > 0.0f) ? (log2f(l) + m_used) * kLn2 : -INFINITY;
+    }
     uint16_t* orow = reinterpret_cast<uint16_t*>(p.out) + w.batch * p.o_sb + w.head * p.o_sh +
                      static_cast<int64_t>(row_g) * p.o_sl;
 #pragma unroll

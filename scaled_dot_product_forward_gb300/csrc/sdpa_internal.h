@@ -16,6 +16,8 @@ struct FwdParams {
   void* out;          // [B, H, L, D] with element strides below (inner stride 1)
   int64_t o_sb, o_sh, o_sl;
   const uint8_t* mask;  // [L, L] row-major bytes, nonzero = removed; null unless mask mode
+  float* lse;           // optional [B, H, L] fp32 log-sum-exp per row (element strides below)
+  int64_t lse_sb, lse_sh, lse_sl;
   int B, H, L;
   int n_tiles;          // ceil(L / 128)
   float scale_log2;     // scale * log2(e)

@@ -116,6 +116,26 @@ def test_args(lib):
     assert call(lib, causal=0, mask=O + 2 * 2 * 3 * L * 64 - 64) == 6   # mask overlaps out
 
 
+def test_lse_argument_checks(lib):
+    import ctypes
+    c = ctypes.CDLL(_build.LIB_PATH)
+    c.sdpa_forward_lse.restype = ctypes.c_int
+    shape = (2, 3, 256, 64)
+    st = contiguous(shape)
+    arr = lambda vals: (ctypes.c_int64 * len(vals))(*vals)
+    def call_lse(lse, lse_stride):
+        return c.sdpa_forward_lse(ctypes.c_void_p(Q), ctypes.c_void_p(K), ctypes.c_void_p(V),
+                                  ctypes.c_void_p(O), ctypes.c_void_p(lse), 0, 4, arr(shape),
+                                  arr(st), arr(st), arr(st), arr(st),
+                                  arr(lse_stride) if lse_stride else None, 1, None,
+                                  ctypes.c_float(float("nan")), None)
+    assert call_lse(0, [768, 256, 1]) == 1                # NULL lse
+    assert call_lse(M, None) == 1                          # NULL strides
+    assert call_lse(M + 2, [768, 256, 1]) == 5             # not 4-byte aligned
+    assert call_lse(M, [768, 0, 1]) == 5                   # zero stride on an extent > 1
+    assert call_lse(O + 64, [768, 256, 1]) == 6            # overlaps out
+
+
 def test_rank3_shape_accepted_by_validation(lib):
     """A rank-3 [H, L, D] call passes validation; without a GPU it then fails
     loudly with SDPA_ERR_CUDA (there is no CPU fallback)."""
