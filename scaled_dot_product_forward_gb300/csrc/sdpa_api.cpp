@@ -48,8 +48,10 @@ EncodeTiledFn get_encode_fn() {
   return fn;
 }
 
-// Per-device answer to "is this an sm_103 part?" (0 unknown, 1 yes, 2 no).
+// Per-device answer to "is this an sm_103 part?" (0 unknown, 1 yes, 2 no),
+// and its SM count (the persistent grid's size).
 std::atomic<int> g_device_ok[64];
+std::atomic<int> g_device_sms[64];
 
 sdpa_status check_device() {
   int dev = 0;
@@ -61,7 +63,11 @@ sdpa_status check_device() {
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
       return SDPA_ERR_CUDA;
-    state = (major == 10 && minor == 3) ? 1 : 2;
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return SDPA_ERR_CUDA;
+    state = (major == 10 && minor == 3 && sms > 0) ? 1 : 2;
+    g_device_sms[dev].store(sms, std::memory_order_relaxed);
     g_device_ok[dev].store(state, std::memory_order_relaxed);
   }
   return state == 1 ? SDPA_OK : SDPA_ERR_DEVICE;
@@ -169,7 +175,7 @@ sdpa_status validate(const void* q, const void* k, const void* v, void* out, sdp
   const int64_t H = shape[rank - 3], L = shape[rank - 2], D = shape[rank - 1];
   if (D != 64 && D != 128) return SDPA_ERR_SHAPE;
   if (L > 0x7fffffffLL - 127) return SDPA_ERR_SHAPE;
-  if (B * H > 0x7fffffffLL / ((L + 127) / 128)) return SDPA_ERR_SHAPE;  // one CTA per tile
+  if (B * H > 0x7fffffffLL / ((L + 127) / 128)) return SDPA_ERR_SHAPE;  // tile and unit counts fit in int
   const void* ptrs[4] = {q, k, v, out};
   const int64_t* strides[4] = {q_stride, k_stride, v_stride, o_stride};
   for (int t = 0; t < 4; ++t) {
@@ -238,6 +244,7 @@ struct Prepared {
   int head_dim;
   bool bf16;
   int device;
+  int sms;  // SM count of that device (persistent grid size)
 };
 
 sdpa_status build_params(const void* q, const void* k, const void* v, void* out, sdpa_dtype dtype,
@@ -251,6 +258,7 @@ sdpa_status build_params(const void* q, const void* k, const void* v, void* out,
   s = check_device();
   if (s != SDPA_OK) return s;
   if (cudaGetDevice(&pr->device) != cudaSuccess) return SDPA_ERR_CUDA;
+  pr->sms = g_device_sms[pr->device].load(std::memory_order_relaxed);
 
   pr->bf16 = (dtype == SDPA_BF16);
   const View* views = pr->views;
@@ -289,7 +297,7 @@ sdpa_status launch_prepared(const Prepared& pr, void* stream) {
   sdpa_impl::FwdParams p = pr.p;
   p.debug_withhold_q = g_withhold_q.load(std::memory_order_relaxed);
   p.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
-  const cudaError_t e = sdpa_impl::launch_forward(p, pr.head_dim, pr.mode, pr.bf16,
+  const cudaError_t e = sdpa_impl::launch_forward(p, pr.head_dim, pr.mode, pr.bf16, pr.sms,
                                                   static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;
 }

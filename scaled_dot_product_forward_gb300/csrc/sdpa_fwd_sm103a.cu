@@ -8,13 +8,17 @@
 // tiles with an online softmax, so the [seq, seq] score matrix never reaches
 // HBM -- but built for Blackwell:
 //
-//   * one CTA per pair of adjacent 128-row query tiles (A = rows 256m..,
-//     B = rows 256m+128..) of one (batch, head); a head's pairs are adjacent
-//     in launch order, heaviest causal pair first, so K/V stay in L2;
-//   * warp 0 (one lane) streams Q_A, Q_B once and rings of K and V tiles
-//     with TMA (128-byte swizzled boxes of 64 x 128 elements), K and V with
-//     their own full/empty barriers;
-//   * warp 1 (one lane) issues tcgen05.mma in the order
+//   * persistent: at most one CTA per SM, each walking a static share of
+//     equal-cost units.  A job is a pair of adjacent 128-row query tiles
+//     (A = rows 256m.., B = rows 256m+128..) of one (batch, head); a unit is
+//     the causal pair P-1-k followed by pair k of the same head, so every
+//     unit costs the same number of key tiles.  Units are head-major, so the
+//     CTAs busy at one time share a few heads' K/V in L2.  The next job's Q
+//     load and first S products overlap the previous job's epilogue;
+//   * warp 0 streams each job's Q_A, Q_B and one ring of K and V tiles that
+//     runs on across jobs, with TMA (128-byte swizzled boxes of 64 x 128
+//     elements), K and V with their own full/empty barriers;
+//   * warp 1 issues tcgen05.mma (one elected lane) in the order
 //       S_A(0) S_B(0) | PV_A(0) S_A(1) PV_B(0) S_B(1) | PV_A(1) S_A(2) ...
 //     so that while one softmax warpgroup works on its tile the tensor core
 //     is busy with the other tile's products; S = Q K^T lands in TMEM, and
@@ -51,10 +55,11 @@ constexpr int kTilesPerCta = 2;
 constexpr int kThreads = 384;  // WG0: TMA warp, MMA warp, 2 spare; WG1: tile A; WG2: tile B
 // Register split: the launch reserves kLaunchRegs per thread (the cap that
 // __launch_bounds__(384, 1) implies); WG0 gives registers back, the two
-// softmax warpgroups take them.  128*56 + 256*224 == 384*168.
+// softmax warpgroups take them.  128*80 + 256*208 == 384*168 (the control
+// warps keep enough for the persistent job loop's counters).
 constexpr uint32_t kLaunchRegs = 168;
-constexpr uint32_t kRegsControl = 56;
-constexpr uint32_t kRegsSoftmax = 224;
+constexpr uint32_t kRegsControl = 80;
+constexpr uint32_t kRegsSoftmax = 208;
 static_assert(128 * kRegsControl + 256 * kRegsSoftmax <= kThreads * kLaunchRegs,
               "register split exceeds the launch allocation");
 constexpr float kRescaleLog2 = 8.0f;  // rescale O only when max grows by > 2^8
@@ -116,10 +121,12 @@ struct Layout {
 constexpr int kMaxStages = 8;
 struct Barriers {
   uint64_t q_full;
+  uint64_t q_empty;  // the job's Q tiles are no longer read (all its S done)
   uint64_t s_full[kTilesPerCta];
   uint64_t p_ready[kTilesPerCta];
   uint64_t o_done[kTilesPerCta];
   uint64_t s_free[kTilesPerCta];  // S(j) loaded by the softmax (early-S plan only)
+  uint64_t o_free[kTilesPerCta];  // the job's O_t read by its epilogue
   uint64_t fin;
   uint64_t k_full[kMaxStages];
   uint64_t v_full[kMaxStages];
@@ -186,7 +193,13 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   }
 }
 
-// Work decomposition shared by every role of a CTA.
+// Work decomposition shared by every role of a CTA.  A job is one pair of
+// adjacent 128-row query tiles of one (batch, head).  A unit is pair P-1-k
+// followed by pair k of the same head (P pairs per head): under the causal
+// mask the two cost 4P + 2 key tiles together whatever k is, so units are
+// equal and a static round-robin assignment of units to persistent CTAs is
+// balanced.  Units are numbered head-major, so the CTAs busy at any moment
+// work on a window of neighbouring heads whose K/V stay in L2.
 struct Work {
   int batch, head;
   int tile[kTilesPerCta];  // query tile index of A and B
@@ -194,12 +207,21 @@ struct Work {
   int n_kv_max;
 };
 
+__host__ __device__ inline int pairs_per_head(int n_tiles) { return (n_tiles + 1) >> 1; }
+__host__ __device__ inline int units_per_head(int n_tiles) {
+  return (pairs_per_head(n_tiles) + 1) >> 1;
+}
+
+// Job `sub` (0 or 1) of unit `u`; false when the unit has no such job (the
+// middle pair of an odd pair count stands alone).
 template <int MODE>
-__device__ __forceinline__ Work make_work(const sdpa_impl::FwdParams& p) {
-  Work w;
-  const int pairs = (p.n_tiles + 1) >> 1;
-  const int bh = static_cast<int>(blockIdx.x / static_cast<unsigned>(pairs));
-  const int pr = pairs - 1 - static_cast<int>(blockIdx.x - bh * pairs);  // heaviest first
+__device__ __forceinline__ bool job_at(const sdpa_impl::FwdParams& p, int u, int sub, Work& w) {
+  const int P = pairs_per_head(p.n_tiles);
+  const int uph = units_per_head(p.n_tiles);
+  const int bh = u / uph;
+  const int k = u - bh * uph;
+  const int pr = (sub == 0) ? (P - 1 - k) : k;
+  if (sub == 1 && pr == P - 1 - k) return false;
   w.batch = bh / p.H;
   w.head = bh - w.batch * p.H;
   w.n_kv_max = 0;
@@ -210,18 +232,40 @@ __device__ __forceinline__ Work make_work(const sdpa_impl::FwdParams& p) {
     w.n_kv[t] = (qt >= p.n_tiles) ? 0 : ((MODE == sdpa_impl::kMaskCausal) ? qt + 1 : p.n_tiles);
     w.n_kv_max = max(w.n_kv_max, w.n_kv[t]);
   }
-  return w;
+  return true;
+}
+
+// Calls f(work) for every job of this CTA, in order; stops when f returns false.
+template <int MODE, typename F>
+__device__ __forceinline__ void for_each_job(const sdpa_impl::FwdParams& p, F&& f) {
+  const int n_units = p.B * p.H * units_per_head(p.n_tiles);
+  for (int u = static_cast<int>(blockIdx.x); u < n_units; u += static_cast<int>(gridDim.x)) {
+#pragma unroll 1
+    for (int sub = 0; sub < 2; ++sub) {
+      Work w;
+      if (job_at<MODE>(p, u, sub, w) && !f(w)) return;
+    }
+  }
 }
 
 // ------------------------------------------------------------ softmax role
 // One warpgroup, one query tile: thread r of the group owns row r (TMEM lane r).
 // Both warpgroups run this one code path (t picks the tile at run time), so
 // the warps sharing an SM sub-partition also share instruction-cache lines.
+// Phase counters that run across the jobs of a persistent CTA (every
+// barrier's phases are consumed strictly in order).
+struct SoftmaxCounters {
+  uint32_t s_seen;   // completions of s_full[t] consumed
+  uint32_t o_seen;   // completions of o_done[t] consumed
+};
+
+// One job of one tile.  Returns false when a wait gave up.
 template <int D, int MODE, bool BF16>
-__device__ __forceinline__ void softmax_role(const sdpa_impl::FwdParams& p, const Work& w, int t,
-                                             Barriers* bars, uint32_t tmem, int wq, int lane) {
+__device__ __forceinline__ bool softmax_job(const sdpa_impl::FwdParams& p, const Work& w, int t,
+                                            Barriers* bars, uint32_t tmem, int wq, int lane,
+                                            SoftmaxCounters& cnt) {
   const int n = t ? w.n_kv[1] : w.n_kv[0];
-  if (n == 0) return;
+  if (n == 0) return true;
   const uint64_t limit = p.wait_limit_ns;
   const int qt = t ? w.tile[1] : w.tile[0];
   using Plan = TmemPlan<D>;
@@ -285,10 +329,11 @@ __device__ __forceinline__ void softmax_role(const sdpa_impl::FwdParams& p, cons
         }
       }
     }
-    if (!warp_wait_phase(&bars->s_full[t], j & 1, bars, limit, kSiteSFull)) {
+    if (!warp_wait_phase(&bars->s_full[t], cnt.s_seen & 1, bars, limit, kSiteSFull)) {
       ok = false;
       break;
     }
+    ++cnt.s_seen;
     tc_fence_after();
     float s[kBlockN];
     {
@@ -392,10 +437,11 @@ __device__ __forceinline__ void softmax_role(const sdpa_impl::FwdParams& p, cons
       // below: once P_j is released, PV_j may complete too, and a parity
       // wait that falls two phases behind its barrier would block until the
       // next phase (a timeout here) instead of returning.
-      if (!warp_wait_phase(&bars->o_done[t], (j - 1) & 1, bars, limit, kSiteODone)) {
+      if (!warp_wait_phase(&bars->o_done[t], cnt.o_seen & 1, bars, limit, kSiteODone)) {
         ok = false;
         break;
       }
+      ++cnt.o_seen;
       tc_fence_after();
       if (__any_sync(0xffffffffu, need)) {
 #pragma unroll
@@ -421,7 +467,10 @@ __device__ __forceinline__ void softmax_role(const sdpa_impl::FwdParams& p, cons
     if (lane == 0) mbar_arrive(&bars->p_ready[t]);  // one arrival per warp
   }
 
-  if (ok && warp_wait_phase(&bars->o_done[t], (n - 1) & 1, bars, limit, kSiteODone)) {
+  if (ok && !warp_wait_phase(&bars->o_done[t], cnt.o_seen & 1, bars, limit, kSiteODone))
+    ok = false;
+  if (ok) {
+    ++cnt.o_seen;
     tc_fence_after();
     const float inv_l = (l > 0.0f) ? (1.0f / l) : 0.0f;
     if (p.lse != nullptr && row_g < p.L) {
@@ -449,8 +498,13 @@ __device__ __forceinline__ void softmax_role(const sdpa_impl::FwdParams& p, cons
           dst[v] = make_uint4(pw[4 * v], pw[4 * v + 1], pw[4 * v + 2], pw[4 * v + 3]);
       }
     }
+    // O_t has been read: the next job's first PV may overwrite it.
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bars->o_free[t]);
   }
   tc_fence_before();
+  return ok;
 }
 
 // ------------------------------------------------------------------ kernel
@@ -468,17 +522,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const Work w = make_work<MODE>(p);
   const uint64_t limit = p.wait_limit_ns;
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
+    mbar_init(&bars->q_empty, 1);
 #pragma unroll
     for (int t = 0; t < kTilesPerCta; ++t) {
       mbar_init(&bars->s_full[t], 1);
       mbar_init(&bars->p_ready[t], kBlockM / 32);
       mbar_init(&bars->o_done[t], 1);
       mbar_init(&bars->s_free[t], kBlockM / 32);
+      mbar_init(&bars->o_free[t], kBlockM / 32);
     }
     mbar_init(&bars->fin, 1);
 #pragma unroll
@@ -519,8 +574,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp >= 4) {
     // ------------------------------------------- softmax / output warps
     regs_increase<kRegsSoftmax>();
-    // warps 4..7 -> tile A, 8..11 -> tile B
-    softmax_role<D, MODE, BF16>(p, w, (warp - 4) >> 2, bars, tmem, warp & 3, lane);
+    // warps 4..7 -> tile A, 8..11 -> tile B; the same jobs as the other roles
+    const int t = (warp - 4) >> 2;
+    SoftmaxCounters cnt{0, 0};
+    for_each_job<MODE>(p, [&](const Work& w) {
+      return softmax_job<D, MODE, BF16>(p, w, t, bars, tmem, warp & 3, lane, cnt);
+    });
   } else {
     regs_decrease<kRegsControl>();
   // Both control warps run their loops with all 32 lanes, so loop variables
@@ -530,53 +589,62 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool leader = elect_one();
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer
-    // Key / value tiles issued so far (a give-up drains them below).
-    int k_end = 0, v_end = 0;
-    if (!p.debug_withhold_q && leader) {
-      const int nq = (w.n_kv[1] > 0) ? 2 : 1;
-      mbar_arrive_expect_tx(&bars->q_full, nq * Lay::kTileBytes);
-      for (int t = 0; t < nq; ++t)
+    // Key/value tiles issued so far over all jobs (ring position) and jobs
+    // whose Q was loaded; a give-up drains what was issued.
+    int g = 0, k_end = 0, v_end = 0, jobs = 0;
+    for_each_job<MODE>(p, [&](const Work& w) -> bool {
+      // The previous job's Q must be consumed (all its S products done).
+      if (jobs > 0 && !warp_wait_phase(&bars->q_empty, (jobs - 1) & 1, bars, limit, kSiteEmpty))
+        return false;
+      if (!p.debug_withhold_q && leader) {
+        const int nq = (w.n_kv[1] > 0) ? 2 : 1;
+        mbar_arrive_expect_tx(&bars->q_full, nq * Lay::kTileBytes);
+        for (int t = 0; t < nq; ++t)
 #pragma unroll
-        for (int c = 0; c < Lay::kChunks; ++c)
-          tma_tile(sQ + t * Lay::kTileBytes + c * Lay::kChunkBytes, &p.tm_q, &bars->q_full,
-                   c * 64, w.tile[t] * kBlockM, w.head, w.batch, p.pos_q);
-    }
-    for (int j = 0; j < w.n_kv_max; ++j) {
-      const int s = j % Lay::kStages;
-      const int use = j / Lay::kStages;
-      if (use > 0 &&
-          !warp_wait_phase(&bars->k_empty[s], (use - 1) & 1, bars, limit, kSiteEmpty))
-        break;
-      if (leader) {
-        mbar_arrive_expect_tx(&bars->k_full[s], Lay::kTileBytes);
-#pragma unroll
-        for (int c = 0; c < Lay::kChunks; ++c)
-          tma_tile(sK + s * Lay::kTileBytes + c * Lay::kChunkBytes, &p.tm_k, &bars->k_full[s],
-                   c * 64, j * kBlockN, w.head, w.batch, p.pos_k);
+          for (int c = 0; c < Lay::kChunks; ++c)
+            tma_tile(sQ + t * Lay::kTileBytes + c * Lay::kChunkBytes, &p.tm_q, &bars->q_full,
+                     c * 64, w.tile[t] * kBlockM, w.head, w.batch, p.pos_q);
       }
-      k_end = j + 1;
-      if (use > 0 &&
-          !warp_wait_phase(&bars->v_empty[s], (use - 1) & 1, bars, limit, kSiteEmpty))
-        break;
-      if (leader) {
-        mbar_arrive_expect_tx(&bars->v_full[s], Lay::kTileBytes);
+      ++jobs;
+      for (int j = 0; j < w.n_kv_max; ++j, ++g) {
+        const int s = g % Lay::kStages;
+        const int use = g / Lay::kStages;
+        if (use > 0 &&
+            !warp_wait_phase(&bars->k_empty[s], (use - 1) & 1, bars, limit, kSiteEmpty))
+          return false;
+        if (leader) {
+          mbar_arrive_expect_tx(&bars->k_full[s], Lay::kTileBytes);
 #pragma unroll
-        for (int c = 0; c < Lay::kChunks; ++c)
-          tma_tile(sV + s * Lay::kTileBytes + c * Lay::kChunkBytes, &p.tm_v, &bars->v_full[s],
-                   c * 64, j * kBlockN, w.head, w.batch, p.pos_v);
+          for (int c = 0; c < Lay::kChunks; ++c)
+            tma_tile(sK + s * Lay::kTileBytes + c * Lay::kChunkBytes, &p.tm_k, &bars->k_full[s],
+                     c * 64, j * kBlockN, w.head, w.batch, p.pos_k);
+        }
+        k_end = g + 1;
+        if (use > 0 &&
+            !warp_wait_phase(&bars->v_empty[s], (use - 1) & 1, bars, limit, kSiteEmpty))
+          return false;
+        if (leader) {
+          mbar_arrive_expect_tx(&bars->v_full[s], Lay::kTileBytes);
+#pragma unroll
+          for (int c = 0; c < Lay::kChunks; ++c)
+            tma_tile(sV + s * Lay::kTileBytes + c * Lay::kChunkBytes, &p.tm_v, &bars->v_full[s],
+                     c * 64, j * kBlockN, w.head, w.batch, p.pos_v);
+        }
+        v_end = g + 1;
       }
-      v_end = j + 1;
-    }
+      return true;
+    });
     // Drain: every load issued must have landed before shared memory is
     // released (only matters when a wait gave up).  The last tile issued into
-    // a stage is the largest j < end with that j % kStages.
+    // a stage is the largest index below the end with that stage.
     for (int j = max(0, k_end - Lay::kStages); j < k_end; ++j)
       wait_phase(&bars->k_full[j % Lay::kStages], (j / Lay::kStages) & 1, bars, limit,
                  kSiteDrain, false);
     for (int j = max(0, v_end - Lay::kStages); j < v_end; ++j)
       wait_phase(&bars->v_full[j % Lay::kStages], (j / Lay::kStages) & 1, bars, limit,
                  kSiteDrain, false);
-    if (!p.debug_withhold_q) wait_phase(&bars->q_full, 0, bars, limit, kSiteDrain, false);
+    if (jobs > 0 && !p.debug_withhold_q)
+      wait_phase(&bars->q_full, (jobs - 1) & 1, bars, limit, kSiteDrain, false);
   } else if (warp == 1) {
     // ------------------------------------------------------- MMA issuer
     constexpr uint32_t idS = idesc_f16_f32acc(BF16, false, kBlockM, kBlockN);
@@ -618,18 +686,55 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit_elect(&bars->o_done[t]);
     };
 
-    bool ok = warp_wait_phase(&bars->q_full, 0, bars, limit, kSiteQFull) &&
-              warp_wait_phase(&bars->k_full[0], 0, bars, limit, kSiteKFull);
-    if (ok) {
+    // Running counters over all jobs: ring position g, jobs done, P-ready
+    // phases consumed per tile, jobs per tile (for o_free), and in the
+    // early-S plan the S(j) loads consumed per tile.
+    int g = 0, jobs = 0;
+    uint32_t p_seen[kTilesPerCta] = {0, 0}, t_jobs[kTilesPerCta] = {0, 0};
+    uint32_t f_seen[kTilesPerCta] = {0, 0};
+    for_each_job<MODE>(p, [&](const Work& w) -> bool {
+      if (!warp_wait_phase(&bars->q_full, jobs & 1, bars, limit, kSiteQFull) ||
+          !warp_wait_phase(&bars->k_full[g % Lay::kStages], (g / Lay::kStages) & 1, bars, limit,
+                           kSiteKFull))
+        return false;
       tc_fence_after();
 #pragma unroll
-      for (int t = 0; t < kTilesPerCta; ++t)
-        if (w.n_kv[t] > 0) issue_s(t, 0);
-      mma_commit_elect(&bars->k_empty[0]);
+      for (int t = 0; t < kTilesPerCta; ++t) {
+        if (w.n_kv[t] == 0) continue;
+        if constexpr (Plan::kEarlyS) {
+          // The previous job's last S_t must be in its softmax's registers.
+          if (t_jobs[t] > 0) {
+            if (!warp_wait_phase(&bars->s_free[t], f_seen[t] & 1, bars, limit, kSiteSFree))
+              return false;
+            ++f_seen[t];
+            tc_fence_after();
+          }
+        }
+        issue_s(t, g % Lay::kStages);
+      }
+      mma_commit_elect(&bars->k_empty[g % Lay::kStages]);
+      if (w.n_kv_max == 1) mma_commit_elect(&bars->q_empty);  // that was the job's last S
       issued_any = true;
+
+      // The first PV_t of a job overwrites O_t: the previous job's epilogue
+      // must have read it.
+      auto pv_ready = [&](int t, int j) -> bool {
+        if (!warp_wait_phase(&bars->p_ready[t], p_seen[t] & 1, bars, limit, kSitePReady))
+          return false;
+        ++p_seen[t];
+        if (j == 0 && t_jobs[t] > 0 &&
+            !warp_wait_phase(&bars->o_free[t], (t_jobs[t] - 1) & 1, bars, limit, kSiteODone))
+          return false;
+        tc_fence_after();
+        return true;
+      };
+
+      bool ok = true;
       for (int j = 0; j < w.n_kv_max && ok; ++j) {
-        const int s = j % Lay::kStages;
-        const int s1 = (j + 1) % Lay::kStages;
+        const int gj = g + j;
+        const int s = gj % Lay::kStages;
+        const int s1 = (gj + 1) % Lay::kStages;
+        const uint32_t ph1 = ((gj + 1) / Lay::kStages) & 1;
         bool k_next = false;
         if constexpr (Plan::kEarlyS) {
           // S(j+1) of both tiles first (each once its softmax has loaded
@@ -638,23 +743,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int t = 0; t < kTilesPerCta; ++t) {
             if (j + 1 >= w.n_kv[t]) continue;
             if (!k_next) {
-              if (!warp_wait_phase(&bars->k_full[s1], ((j + 1) / Lay::kStages) & 1, bars, limit,
-                                   kSiteKFull)) {
+              if (!warp_wait_phase(&bars->k_full[s1], ph1, bars, limit, kSiteKFull)) {
                 ok = false;
                 break;
               }
               k_next = true;
             }
-            if (!warp_wait_phase(&bars->s_free[t], j & 1, bars, limit, kSiteSFree)) {
+            if (!warp_wait_phase(&bars->s_free[t], f_seen[t] & 1, bars, limit, kSiteSFree)) {
               ok = false;
               break;
             }
+            ++f_seen[t];
             tc_fence_after();
             issue_s(t, s1);
           }
           if (!ok) break;
           if (k_next) mma_commit_elect(&bars->k_empty[s1]);
-          if (!warp_wait_phase(&bars->v_full[s], (j / Lay::kStages) & 1, bars, limit,
+          if (j + 2 == w.n_kv_max) mma_commit_elect(&bars->q_empty);  // job's last S issued
+          if (!warp_wait_phase(&bars->v_full[s], (gj / Lay::kStages) & 1, bars, limit,
                                kSiteVFull)) {
             ok = false;
             break;
@@ -662,49 +768,54 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int t = 0; t < kTilesPerCta; ++t) {
             if (j >= w.n_kv[t]) continue;
-            if (!warp_wait_phase(&bars->p_ready[t], j & 1, bars, limit, kSitePReady)) {
+            if (!pv_ready(t, j)) {
               ok = false;
               break;
             }
-            tc_fence_after();
             issue_pv(t, s, j > 0);
           }
           if (!ok) break;
           mma_commit_elect(&bars->v_empty[s]);
         } else {
-        if (!warp_wait_phase(&bars->v_full[s], (j / Lay::kStages) & 1, bars, limit,
-                             kSiteVFull)) {
-          ok = false;
-          break;
-        }
-#pragma unroll
-        for (int t = 0; t < kTilesPerCta; ++t) {
-          if (j >= w.n_kv[t]) continue;
-          if (!warp_wait_phase(&bars->p_ready[t], j & 1, bars, limit, kSitePReady)) {
+          if (!warp_wait_phase(&bars->v_full[s], (gj / Lay::kStages) & 1, bars, limit,
+                               kSiteVFull)) {
             ok = false;
             break;
           }
-          tc_fence_after();
-          issue_pv(t, s, j > 0);
-          if (j + 1 < w.n_kv[t]) {
-            if (!k_next) {
-              if (!warp_wait_phase(&bars->k_full[s1], ((j + 1) / Lay::kStages) & 1, bars, limit,
-                                   kSiteKFull)) {
-                ok = false;
-                break;
-              }
-              tc_fence_after();
-              k_next = true;
+#pragma unroll
+          for (int t = 0; t < kTilesPerCta; ++t) {
+            if (j >= w.n_kv[t]) continue;
+            if (!pv_ready(t, j)) {
+              ok = false;
+              break;
             }
-            issue_s(t, s1);
+            issue_pv(t, s, j > 0);
+            if (j + 1 < w.n_kv[t]) {
+              if (!k_next) {
+                if (!warp_wait_phase(&bars->k_full[s1], ph1, bars, limit, kSiteKFull)) {
+                  ok = false;
+                  break;
+                }
+                tc_fence_after();
+                k_next = true;
+              }
+              issue_s(t, s1);
+            }
           }
+          if (!ok) break;
+          mma_commit_elect(&bars->v_empty[s]);
+          if (k_next) mma_commit_elect(&bars->k_empty[s1]);
+          if (j + 2 == w.n_kv_max) mma_commit_elect(&bars->q_empty);  // job's last S issued
         }
-        if (!ok) break;
-        mma_commit_elect(&bars->v_empty[s]);
-        if (k_next) mma_commit_elect(&bars->k_empty[s1]);
-        }  // plan with P written over S
       }
-    }
+      if (!ok) return false;
+      g += w.n_kv_max;
+      ++jobs;
+#pragma unroll
+      for (int t = 0; t < kTilesPerCta; ++t)
+        if (w.n_kv[t] > 0) ++t_jobs[t];
+      return true;
+    });
     if (issued_any) {
       // Everything issued must finish before TMEM is released.
       mma_commit_elect(&bars->fin);
@@ -722,7 +833,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int D, int MODE, bool BF16>
-cudaError_t launch_one(const sdpa_impl::FwdParams& p, cudaStream_t stream) {
+cudaError_t launch_one(const sdpa_impl::FwdParams& p, int max_ctas, cudaStream_t stream) {
   auto kern = sdpa_fwd_kernel<D, MODE, BF16>;
   constexpr int smem = Layout<D>::kTotal;
   static bool configured = false;  // one attribute call per instantiation
@@ -738,12 +849,17 @@ cudaError_t launch_one(const sdpa_impl::FwdParams& p, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  const unsigned pairs = static_cast<unsigned>((p.n_tiles + 1) / 2);
+  // Persistent grid: one CTA per SM at most, each walking its share of the
+  // equal-cost units.
+  const long long n_units =
+      static_cast<long long>(p.B) * p.H * units_per_head(p.n_tiles);
+  const unsigned grid = static_cast<unsigned>(
+      n_units < static_cast<long long>(max_ctas) ? n_units : static_cast<long long>(max_ctas));
   // Programmatic dependent launch: this grid's set-up may start while the
   // previous kernel in the stream drains; the kernel waits for it
   // (griddepcontrol.wait) before its first global-memory access.
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(pairs * static_cast<unsigned>(p.B * p.H));
+  cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
@@ -756,14 +872,15 @@ cudaError_t launch_one(const sdpa_impl::FwdParams& p, cudaStream_t stream) {
 }
 
 template <int D, bool BF16>
-cudaError_t launch_mode(const sdpa_impl::FwdParams& p, int mode, cudaStream_t stream) {
+cudaError_t launch_mode(const sdpa_impl::FwdParams& p, int mode, int max_ctas,
+                        cudaStream_t stream) {
   switch (mode) {
     case sdpa_impl::kMaskCausal:
-      return launch_one<D, sdpa_impl::kMaskCausal, BF16>(p, stream);
+      return launch_one<D, sdpa_impl::kMaskCausal, BF16>(p, max_ctas, stream);
     case sdpa_impl::kMaskExplicit:
-      return launch_one<D, sdpa_impl::kMaskExplicit, BF16>(p, stream);
+      return launch_one<D, sdpa_impl::kMaskExplicit, BF16>(p, max_ctas, stream);
     default:
-      return launch_one<D, sdpa_impl::kMaskNone, BF16>(p, stream);
+      return launch_one<D, sdpa_impl::kMaskNone, BF16>(p, max_ctas, stream);
   }
 }
 
@@ -795,12 +912,13 @@ cudaError_t launch_exp2_poly(const float* x, float* y, int64_t n, cudaStream_t s
 }
 
 cudaError_t launch_forward(const FwdParams& p, int head_dim, int mask_mode, bool bf16,
-                           cudaStream_t stream) {
+                           int max_ctas, cudaStream_t stream) {
+  if (max_ctas < 1) return cudaErrorInvalidValue;
   if (head_dim == 64)
-    return bf16 ? launch_mode<64, true>(p, mask_mode, stream)
-                : launch_mode<64, false>(p, mask_mode, stream);
-  return bf16 ? launch_mode<128, true>(p, mask_mode, stream)
-              : launch_mode<128, false>(p, mask_mode, stream);
+    return bf16 ? launch_mode<64, true>(p, mask_mode, max_ctas, stream)
+                : launch_mode<64, false>(p, mask_mode, max_ctas, stream);
+  return bf16 ? launch_mode<128, true>(p, mask_mode, max_ctas, stream)
+              : launch_mode<128, false>(p, mask_mode, max_ctas, stream);
 }
 
 cudaError_t read_and_clear_device_status(cudaStream_t stream, unsigned int* status) {

@@ -31,8 +31,10 @@ enum MaskMode : int { kMaskNone = 0, kMaskCausal = 1, kMaskExplicit = 2 };
 
 // Launches the fused forward kernel for (head_dim, mask mode, dtype) on
 // `stream`.  Returns the CUDA error of the launch.
+// Launches the persistent forward kernel with at most max_ctas CTAs (one per
+// SM: pass the device's SM count).
 cudaError_t launch_forward(const FwdParams& p, int head_dim, int mask_mode, bool bf16,
-                           cudaStream_t stream);
+                           int max_ctas, cudaStream_t stream);
 
 // Test hook: y[i] = 2^x[i] through the kernel's FMA-pipe polynomial.
 cudaError_t launch_exp2_poly(const float* x, float* y, int64_t n, cudaStream_t stream);
