@@ -432,17 +432,22 @@ __device__ __forceinline__ bool softmax_job(const sdpa_impl::FwdParams& p, const
     l += rs[0] + rs[1];
 
     if (j > 0) {
-      // Consume PV_{j-1}'s completion in order; it is needed anyway before O
-      // may be rescaled.  This wait must stay BEFORE the p_ready arrival
-      // below: once P_j is released, PV_j may complete too, and a parity
-      // wait that falls two phases behind its barrier would block until the
-      // next phase (a timeout here) instead of returning.
-      if (!warp_wait_phase(&bars->o_done[t], cnt.o_seen & 1, bars, limit, kSiteODone)) {
-        ok = false;
-        break;
+      // PV_{j-1} must have completed before O is rescaled or P_j replaces
+      // P_{j-1}.  Where P is written over S, S_j was issued after PV_{j-1}
+      // and the tensor pipe completes in issue order, so s_full(j) already
+      // implies it: that phase of o_done is complete and is only counted.
+      // Otherwise it is waited for here, in order and BEFORE the p_ready
+      // arrival below: once P_j is released PV_j may complete too, and a
+      // parity wait that falls two phases behind its barrier would block
+      // until the next phase (a timeout here) instead of returning.
+      if constexpr (Plan::kEarlyS) {
+        if (!warp_wait_phase(&bars->o_done[t], cnt.o_seen & 1, bars, limit, kSiteODone)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
       }
       ++cnt.o_seen;
-      tc_fence_after();
       if (__any_sync(0xffffffffu, need)) {
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
@@ -458,7 +463,7 @@ __device__ __forceinline__ bool softmax_job(const sdpa_impl::FwdParams& p, const
     }
     // P_j goes into the P buffer -- the first 64 columns of this tile's score
     // buffer, or its own buffer in the early-S plan (free again: PV_{j-1}
-    // has completed, waited for above).
+    // has completed, see above).
     tmem_st32(tP + 0, pk);
     tmem_st32(tP + 32, pk + 32);
     tmem_st_wait();
