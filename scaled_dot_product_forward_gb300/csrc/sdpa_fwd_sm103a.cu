@@ -109,11 +109,17 @@ struct Layout {
   static constexpr int kChunks = D / 64;               // 128-byte swizzle atoms along D
   static constexpr int kChunkBytes = kBlockM * 128;    // one 128-row x 64-element box
   static constexpr int kTileBytes = kChunks * kChunkBytes;
-  static constexpr int kStages = (D == 64) ? 6 : 2;    // K/V ring depth
+  // Ring depths.  With D = 128 there is room for five 32 KB tiles beside Q
+  // (64 KB).  A stage of K is refilled once S of both tiles has read it and
+  // that tile is needed again 2.5 products-pairs later, earlier than V
+  // (refilled after PV of both tiles, needed three pairs later), so K gets
+  // the third stage.
+  static constexpr int kKStages = (D == 64) ? 6 : 3;
+  static constexpr int kVStages = (D == 64) ? 6 : 2;
   static constexpr int kQ = 0;
   static constexpr int kK = kQ + kTilesPerCta * kTileBytes;
-  static constexpr int kV = kK + kStages * kTileBytes;
-  static constexpr int kBar = kV + kStages * kTileBytes;
+  static constexpr int kV = kK + kKStages * kTileBytes;
+  static constexpr int kBar = kV + kVStages * kTileBytes;
   static constexpr int kBarBytes = 512;
   static constexpr int kTotal = kBar + kBarBytes + 1024;  // + slack for 1 KB alignment
 };
@@ -138,7 +144,9 @@ struct Barriers {
 static_assert(sizeof(Barriers) <= 512, "barrier block too large");
 static_assert(Layout<128>::kTotal <= 227 * 1024, "shared memory over the per-CTA limit");
 static_assert(Layout<64>::kTotal <= 227 * 1024, "shared memory over the per-CTA limit");
-static_assert(Layout<64>::kStages <= kMaxStages && Layout<128>::kStages <= kMaxStages, "ring");
+static_assert(Layout<64>::kKStages <= kMaxStages && Layout<128>::kKStages <= kMaxStages &&
+                  Layout<64>::kVStages <= kMaxStages && Layout<128>::kVStages <= kMaxStages,
+              "ring");
 
 // Bounded wait on one barrier phase.  Returns false when the wait gave up:
 // either another role already raised the CTA abort flag (honour_abort), or
@@ -542,10 +550,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(&bars->fin, 1);
 #pragma unroll
-    for (int s = 0; s < Lay::kStages; ++s) {
+    for (int s = 0; s < Lay::kKStages; ++s) {
       mbar_init(&bars->k_full[s], 1);
-      mbar_init(&bars->v_full[s], 1);
       mbar_init(&bars->k_empty[s], 1);
+    }
+#pragma unroll
+    for (int s = 0; s < Lay::kVStages; ++s) {
+      mbar_init(&bars->v_full[s], 1);
       mbar_init(&bars->v_empty[s], 1);
     }
     bars->abort_flag = 0;
@@ -612,8 +623,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       ++jobs;
       for (int j = 0; j < w.n_kv_max; ++j, ++g) {
-        const int s = g % Lay::kStages;
-        const int use = g / Lay::kStages;
+        const int s = g % Lay::kKStages;
+        const int use = g / Lay::kKStages;
         if (use > 0 &&
             !warp_wait_phase(&bars->k_empty[s], (use - 1) & 1, bars, limit, kSiteEmpty))
           return false;
@@ -625,14 +636,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                      c * 64, j * kBlockN, w.head, w.batch, p.pos_k);
         }
         k_end = g + 1;
-        if (use > 0 &&
-            !warp_wait_phase(&bars->v_empty[s], (use - 1) & 1, bars, limit, kSiteEmpty))
+        const int sv = g % Lay::kVStages;
+        const int use_v = g / Lay::kVStages;
+        if (use_v > 0 &&
+            !warp_wait_phase(&bars->v_empty[sv], (use_v - 1) & 1, bars, limit, kSiteEmpty))
           return false;
         if (leader) {
-          mbar_arrive_expect_tx(&bars->v_full[s], Lay::kTileBytes);
+          mbar_arrive_expect_tx(&bars->v_full[sv], Lay::kTileBytes);
 #pragma unroll
           for (int c = 0; c < Lay::kChunks; ++c)
-            tma_tile(sV + s * Lay::kTileBytes + c * Lay::kChunkBytes, &p.tm_v, &bars->v_full[s],
+            tma_tile(sV + sv * Lay::kTileBytes + c * Lay::kChunkBytes, &p.tm_v, &bars->v_full[sv],
                      c * 64, j * kBlockN, w.head, w.batch, p.pos_v);
         }
         v_end = g + 1;
@@ -642,11 +655,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Drain: every load issued must have landed before shared memory is
     // released (only matters when a wait gave up).  The last tile issued into
     // a stage is the largest index below the end with that stage.
-    for (int j = max(0, k_end - Lay::kStages); j < k_end; ++j)
-      wait_phase(&bars->k_full[j % Lay::kStages], (j / Lay::kStages) & 1, bars, limit,
+    for (int j = max(0, k_end - Lay::kKStages); j < k_end; ++j)
+      wait_phase(&bars->k_full[j % Lay::kKStages], (j / Lay::kKStages) & 1, bars, limit,
                  kSiteDrain, false);
-    for (int j = max(0, v_end - Lay::kStages); j < v_end; ++j)
-      wait_phase(&bars->v_full[j % Lay::kStages], (j / Lay::kStages) & 1, bars, limit,
+    for (int j = max(0, v_end - Lay::kVStages); j < v_end; ++j)
+      wait_phase(&bars->v_full[j % Lay::kVStages], (j / Lay::kVStages) & 1, bars, limit,
                  kSiteDrain, false);
     if (jobs > 0 && !p.debug_withhold_q)
       wait_phase(&bars->q_full, (jobs - 1) & 1, bars, limit, kSiteDrain, false);
@@ -699,7 +712,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t f_seen[kTilesPerCta] = {0, 0};
     for_each_job<MODE>(p, [&](const Work& w) -> bool {
       if (!warp_wait_phase(&bars->q_full, jobs & 1, bars, limit, kSiteQFull) ||
-          !warp_wait_phase(&bars->k_full[g % Lay::kStages], (g / Lay::kStages) & 1, bars, limit,
+          !warp_wait_phase(&bars->k_full[g % Lay::kKStages], (g / Lay::kKStages) & 1, bars, limit,
                            kSiteKFull))
         return false;
       tc_fence_after();
@@ -715,9 +728,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
           }
         }
-        issue_s(t, g % Lay::kStages);
+        issue_s(t, g % Lay::kKStages);
       }
-      mma_commit_elect(&bars->k_empty[g % Lay::kStages]);
+      mma_commit_elect(&bars->k_empty[g % Lay::kKStages]);
       if (w.n_kv_max == 1) mma_commit_elect(&bars->q_empty);  // that was the job's last S
       issued_any = true;
 
@@ -737,9 +750,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int j = 0; j < w.n_kv_max && ok; ++j) {
         const int gj = g + j;
-        const int s = gj % Lay::kStages;
-        const int s1 = (gj + 1) % Lay::kStages;
-        const uint32_t ph1 = ((gj + 1) / Lay::kStages) & 1;
+        const int s = gj % Lay::kVStages;   // V(j)
+        const int s1 = (gj + 1) % Lay::kKStages;  // K(j+1)
+        const uint32_t ph1 = ((gj + 1) / Lay::kKStages) & 1;
         bool k_next = false;
         if constexpr (Plan::kEarlyS) {
           // S(j+1) of both tiles first (each once its softmax has loaded
@@ -765,7 +778,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ok) break;
           if (k_next) mma_commit_elect(&bars->k_empty[s1]);
           if (j + 2 == w.n_kv_max) mma_commit_elect(&bars->q_empty);  // job's last S issued
-          if (!warp_wait_phase(&bars->v_full[s], (gj / Lay::kStages) & 1, bars, limit,
+          if (!warp_wait_phase(&bars->v_full[s], (gj / Lay::kVStages) & 1, bars, limit,
                                kSiteVFull)) {
             ok = false;
             break;
@@ -782,7 +795,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ok) break;
           mma_commit_elect(&bars->v_empty[s]);
         } else {
-          if (!warp_wait_phase(&bars->v_full[s], (gj / Lay::kStages) & 1, bars, limit,
+          if (!warp_wait_phase(&bars->v_full[s], (gj / Lay::kVStages) & 1, bars, limit,
                                kSiteVFull)) {
             ok = false;
             break;
