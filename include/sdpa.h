@@ -171,6 +171,46 @@ SDPA_API sdpa_status sdpa_forward_lse(const void* q, const void* k, const void* 
                                       int is_causal, const uint8_t* mask, float scale,
                                       void* stream);
 
+/*
+ * sdpa_forward_varlen -- packed variable-length sequences.  Several
+ * documents are stored one after another along the token axis and
+ * described by cumulative offsets, the cu_seqlens arrays that the varlen
+ * kernels on the FlashInfer pull-request page take ("FlashInfer, Cake DSA
+ * kernel optimization", blog.secrett2633.cloud, section 3 on varlen index
+ * preparation).  Each document attends only to itself: sequence i is rows
+ * [cu_seqlens[i], cu_seqlens[i+1]) of q, k and v, and its output rows are
+ * exactly what sdpa_forward returns for that slice alone (the same kernel
+ * and per-tile arithmetic, so bit-identical).  Queries and keys share one
+ * offsets array (self-attention; causal means key j <= query i within the
+ * document).
+ *
+ * q, k, v, out : DEVICE [total, H, D] 16-bit tensors of type `dtype`.
+ * *_stride     : 3 strides in ELEMENTS in (token, head, dim) order; the dim
+ *                stride must be 1, the others multiples of 8 elements.
+ * lse          : NULL, or DEVICE fp32 [H, total] (lse_stride: 2 strides, head
+ *                then token), the per-row log-sum-exp as in sdpa_forward_lse.
+ * cu_seqlens   : DEVICE int32 [n_seqs + 1], 4-byte aligned, nondecreasing,
+ *                cu_seqlens[0] = 0 and cu_seqlens[n_seqs] = total.  The
+ *                kernel uses the running maximum of the offsets clamped to
+ *                [0, total] (the identity for valid offsets), so bad offsets
+ *                cannot make it read or write outside the buffers or make
+ *                two sequences overlap; rows covered by no sequence are
+ *                left unwritten.
+ * max_seqlen   : an upper bound on the sequence lengths; it only sizes the
+ *                grid (a smaller value gives fewer CTAs, never missed work).
+ * Explicit masks are not supported here (is_causal or no mask).  Errors as
+ * sdpa_forward, plus SDPA_ERR_SHAPE for n_seqs < 1 or max_seqlen < 1 and
+ * SDPA_ERR_ARG when out or lse overlaps cu_seqlens.
+ */
+SDPA_API sdpa_status sdpa_forward_varlen(const void* q, const void* k, const void* v, void* out,
+                                         float* lse, sdpa_dtype dtype, int64_t total,
+                                         int64_t n_heads, int64_t head_dim,
+                                         const int64_t* q_stride, const int64_t* k_stride,
+                                         const int64_t* v_stride, const int64_t* o_stride,
+                                         const int64_t* lse_stride, const int32_t* cu_seqlens,
+                                         int64_t n_seqs, int64_t max_seqlen, int is_causal,
+                                         float scale, void* stream);
+
 /* Adds (lse != NULL) or removes (lse == NULL) the log-sum-exp output of a
  * plan; same layout rules as sdpa_forward_lse. */
 SDPA_API sdpa_status sdpa_plan_set_lse(sdpa_plan* plan, float* lse, const int64_t* lse_stride);

@@ -177,3 +177,36 @@ def sdpa_rows(q, k, v, rows, mask=None, is_causal=False, scale=None,
     if rc != 0:
         raise RuntimeError("oracle_sdpa_rows_fp64 failed (row index out of range?)")
     return (out, lse) if return_lse else out
+
+
+def sdpa_varlen(q, k, v, cu_seqlens, is_causal=False, scale=None, return_lse=False):
+    """Packed documents: ``q, k, v`` are [total, H, D] with document i in rows
+    ``[cu_seqlens[i], cu_seqlens[i+1])``, as the varlen kernels on the
+    FlashInfer pull-request page ("FlashInfer, Cake DSA kernel optimization",
+    blog.secrett2633.cloud, section 3) describe their per-document rows with
+    cumulative offsets.  Each document is attended on its own (the attention
+    above, applied to its slice); rows outside every document stay NaN.
+    Returns [total, H, D] fp64 (and the log-sum-exp [H, total])."""
+    q, k, v = _as_f64(q), _as_f64(k), _as_f64(v)
+    if q.ndim != 3 or not (q.shape == k.shape == v.shape):
+        raise ValueError("q, k, v must share one [total, H, D] shape")
+    cu = np.asarray(cu_seqlens, dtype=np.int64).reshape(-1)
+    total, H, D = q.shape
+    if cu.size < 2 or cu[0] < 0 or cu[-1] > total or np.any(np.diff(cu) < 0):
+        raise ValueError("cu_seqlens must be nondecreasing within [0, total]")
+    out = np.full(q.shape, np.nan)
+    lse = np.full((H, total), np.nan) if return_lse else None
+    for a, b in zip(cu[:-1], cu[1:]):
+        if b == a:
+            continue
+        sl = slice(int(a), int(b))
+        # [len, H, D] -> [H, len, D]
+        qs, ks, vs = (np.ascontiguousarray(x[sl].transpose(1, 0, 2)) for x in (q, k, v))
+        r = sdpa(qs, ks, vs, is_causal=is_causal, scale=scale, return_lse=return_lse)
+        if return_lse:
+            o, l = r
+            lse[:, sl] = l
+        else:
+            o = r
+        out[sl] = o.transpose(1, 0, 2)
+    return (out, lse) if return_lse else out

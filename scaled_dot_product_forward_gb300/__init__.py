@@ -20,7 +20,7 @@ from . import _build
 __all__ = ["sdpa_forward", "sdpa_forward_raw", "sdpa_status_string", "sdpa_last_device_status",
            "sdpa_version", "SdpaError", "load_library", "LIB_PATH", "STATUS",
            "sdpa_debug_set_wait_limit_ns", "sdpa_debug_withhold_q_load", "sdpa_debug_exp2_poly",
-           "SdpaPlan"]
+           "sdpa_forward_varlen", "SdpaPlan"]
 
 LIB_PATH = _build.LIB_PATH
 
@@ -84,6 +84,11 @@ def load_library(path: str | None = None):
     lib.sdpa_forward_lse.restype = ctypes.c_int
     lib.sdpa_plan_set_lse.argtypes = [vp, vp, i64p]
     lib.sdpa_plan_set_lse.restype = ctypes.c_int
+    lib.sdpa_forward_varlen.argtypes = [vp, vp, vp, vp, vp, ctypes.c_int, ctypes.c_int64,
+                                        ctypes.c_int64, ctypes.c_int64, i64p, i64p, i64p, i64p,
+                                        i64p, vp, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
+                                        ctypes.c_float, vp]
+    lib.sdpa_forward_varlen.restype = ctypes.c_int
     if path is None:
         _lib = lib
     return lib
@@ -195,6 +200,50 @@ def sdpa_forward(q, k, v, out=None, *, is_causal: bool = False, mask=None, scale
     if rc != 0:
         raise SdpaError(rc, "sdpa_forward_lse")
     return out, lse
+
+
+def sdpa_forward_varlen(q, k, v, cu_seqlens, max_seqlen, out=None, *, is_causal: bool = False,
+                        scale=None, stream=None, return_lse: bool = False, lse=None):
+    """Packed variable-length sequences (sdpa_forward_varlen).
+
+    q, k, v: [total, H, D] bf16/fp16 CUDA tensors (any strides with the last
+    one 1); cu_seqlens: int32 CUDA tensor [n_seqs + 1] of row offsets, each
+    sequence attending only to itself; max_seqlen: an upper bound on the
+    lengths.  Returns ``out`` [total, H, D], or ``(out, lse)`` with lse fp32
+    [H, total].
+    """
+    import torch
+
+    dt = _dtype_code(q)
+    if k.dtype != q.dtype or v.dtype != q.dtype:
+        raise SdpaError(4)
+    if q.dim() != 3 or q.shape != k.shape or q.shape != v.shape:
+        raise SdpaError(3)
+    if cu_seqlens.dtype != torch.int32 or cu_seqlens.dim() != 1 or not cu_seqlens.is_contiguous():
+        raise SdpaError(5)
+    if out is None:
+        out = torch.empty_like(q, memory_format=torch.contiguous_format)
+    elif out.dtype != q.dtype or out.shape != q.shape:
+        raise SdpaError(3)
+    want_lse = return_lse or lse is not None
+    if want_lse:
+        if lse is None:
+            lse = torch.empty((q.shape[1], q.shape[0]), dtype=torch.float32, device=q.device)
+        elif lse.dtype != torch.float32 or tuple(lse.shape) != (q.shape[1], q.shape[0]):
+            raise SdpaError(3)
+    s = float("nan") if scale is None else float(scale)
+    st = (stream if stream is not None else torch.cuda.current_stream(q.device)).cuda_stream
+    rc = load_library().sdpa_forward_varlen(
+        ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k.data_ptr()),
+        ctypes.c_void_p(v.data_ptr()), ctypes.c_void_p(out.data_ptr()),
+        ctypes.c_void_p(lse.data_ptr()) if want_lse else None, dt, q.shape[0], q.shape[1],
+        q.shape[2], _arr(q.stride()), _arr(k.stride()), _arr(v.stride()), _arr(out.stride()),
+        _arr(lse.stride()) if want_lse else None, ctypes.c_void_p(cu_seqlens.data_ptr()),
+        cu_seqlens.numel() - 1, int(max_seqlen), 1 if is_causal else 0, ctypes.c_float(s),
+        ctypes.c_void_p(st) if st else None)
+    if rc != 0:
+        raise SdpaError(rc, "sdpa_forward_varlen")
+    return (out, lse) if want_lse else out
 
 
 def _dtype_code(q):

@@ -367,6 +367,64 @@ sdpa_status sdpa_forward_lse(const void* q, const void* k, const void* v, void* 
   return launch_prepared(pr, stream);
 }
 
+sdpa_status sdpa_forward_varlen(const void* q, const void* k, const void* v, void* out,
+                                float* lse, sdpa_dtype dtype, int64_t total, int64_t n_heads,
+                                int64_t head_dim, const int64_t* q_stride,
+                                const int64_t* k_stride, const int64_t* v_stride,
+                                const int64_t* o_stride, const int64_t* lse_stride,
+                                const int32_t* cu_seqlens, int64_t n_seqs, int64_t max_seqlen,
+                                int is_causal, float scale, void* stream) {
+  if (!cu_seqlens || !q_stride || !k_stride || !v_stride || !o_stride) return SDPA_ERR_NULL;
+  if (n_seqs < 1 || n_seqs > 0x7fffffffLL - 64 || max_seqlen < 1) return SDPA_ERR_SHAPE;
+  if ((reinterpret_cast<uintptr_t>(cu_seqlens) & 3u) != 0) return SDPA_ERR_LAYOUT;
+  // [total, H, D] with (token, head, dim) strides is the rank-3 view
+  // [H, total, D] with (head, token, dim) strides.
+  const int64_t shape[3] = {n_heads, total, head_dim};
+  const int64_t qs[3] = {q_stride[1], q_stride[0], q_stride[2]};
+  const int64_t ks[3] = {k_stride[1], k_stride[0], k_stride[2]};
+  const int64_t vs[3] = {v_stride[1], v_stride[0], v_stride[2]};
+  const int64_t os[3] = {o_stride[1], o_stride[0], o_stride[2]};
+  Prepared pr;
+  sdpa_status s = validate(q, k, v, out, dtype, 3, shape, qs, ks, vs, os, is_causal, nullptr,
+                           scale, pr.views);
+  if (s != SDPA_OK) return s;
+  {
+    // the offsets are read by the kernel while it writes out
+    uintptr_t o0, o1;
+    span_of(pr.views[3], &o0, &o1);
+    const uintptr_t c0 = reinterpret_cast<uintptr_t>(cu_seqlens);
+    if (overlaps(o0, o1, c0, c0 + 4 * static_cast<uintptr_t>(n_seqs + 1))) return SDPA_ERR_ARG;
+  }
+  int64_t ls[3] = {0, 0, 0};
+  if (lse) {
+    if (!lse_stride) return SDPA_ERR_NULL;
+    if ((s = check_lse(lse, 3, shape, lse_stride, pr.views, nullptr, ls)) != SDPA_OK) return s;
+    const uintptr_t l0 = reinterpret_cast<uintptr_t>(lse);
+    const uintptr_t c0 = reinterpret_cast<uintptr_t>(cu_seqlens);
+    if (overlaps(l0, l0 + 4 * static_cast<uintptr_t>((n_heads - 1) * ls[1] + (total - 1) * ls[2] + 1),
+                 c0, c0 + 4 * static_cast<uintptr_t>(n_seqs + 1)))
+      return SDPA_ERR_ARG;
+  }
+  s = build_params(q, k, v, out, dtype, 3, shape, qs, ks, vs, os, is_causal, nullptr, scale, &pr);
+  if (s != SDPA_OK) return s;
+  pr.p.cu_seqlens = cu_seqlens;
+  pr.p.n_seqs = static_cast<int>(n_seqs);
+  // Grid bound: every sequence at most max_seqlen rows (a smaller bound only
+  // means fewer CTAs, never missed work: each CTA walks all its units).
+  const int64_t ml = max_seqlen < total ? max_seqlen : total;
+  const int64_t uph = (((ml + 127) / 128 + 1) / 2 + 1) / 2;
+  const double bound = static_cast<double>(n_seqs) * static_cast<double>(n_heads) *
+                       static_cast<double>(uph);
+  pr.p.max_units = bound > 2.0e9 ? 2000000000LL : static_cast<long long>(bound);
+  if (lse) {
+    pr.p.lse = lse;
+    pr.p.lse_sb = ls[0];
+    pr.p.lse_sh = ls[1];
+    pr.p.lse_sl = ls[2];
+  }
+  return launch_prepared(pr, stream);
+}
+
 sdpa_status sdpa_plan_create(sdpa_plan** plan, const void* q, const void* k, const void* v,
                              void* out, sdpa_dtype dtype, int rank, const int64_t* shape,
                              const int64_t* q_stride, const int64_t* k_stride,

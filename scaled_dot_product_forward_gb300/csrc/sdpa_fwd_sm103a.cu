@@ -202,15 +202,18 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
 }
 
 // Work decomposition shared by every role of a CTA.  A job is one pair of
-// adjacent 128-row query tiles of one (batch, head).  A unit is pair P-1-k
-// followed by pair k of the same head (P pairs per head): under the causal
-// mask the two cost 4P + 2 key tiles together whatever k is, so units are
-// equal and a static round-robin assignment of units to persistent CTAs is
-// balanced.  Units are numbered head-major, so the CTAs busy at any moment
-// work on a window of neighbouring heads whose K/V stay in L2.
+// adjacent 128-row query tiles of one (sequence, head).  A unit is pair
+// P-1-k followed by pair k of the same head (P pairs per head): under the
+// causal mask the two cost 4P + 2 key tiles together whatever k is, so units
+// of one sequence length are equal and a static round-robin assignment of
+// units to persistent CTAs is balanced.  Units are numbered head-major, so
+// the CTAs busy at any moment work on a window of neighbouring heads whose
+// K/V stay in L2.  Every role walks the same sequence of jobs.
 struct Work {
-  int batch, head;
-  int tile[kTilesPerCta];  // query tile index of A and B
+  int batch, head;         // tensor-map coordinates (batch is 0 for packed sequences)
+  int row0;                // first row of the sequence along L (packed: its offset)
+  int len;                 // rows (= keys) of the sequence
+  int tile[kTilesPerCta];  // query tile index of A and B within the sequence
   int n_kv[kTilesPerCta];  // key tiles each query tile visits (0: tile absent)
   int n_kv_max;
 };
@@ -219,39 +222,126 @@ __host__ __device__ inline int pairs_per_head(int n_tiles) { return (n_tiles + 1
 __host__ __device__ inline int units_per_head(int n_tiles) {
   return (pairs_per_head(n_tiles) + 1) >> 1;
 }
+__host__ __device__ inline int tiles_of(int len) { return (len + kBlockM - 1) / kBlockM; }
 
-// Job `sub` (0 or 1) of unit `u`; false when the unit has no such job (the
-// middle pair of an odd pair count stands alone).
+// Job `sub` (0 or 1) of unit k of one (sequence, head) with n_tiles tiles;
+// false when the unit has no such job (the middle pair of an odd pair count
+// stands alone).  Fills the tile fields of w.
 template <int MODE>
-__device__ __forceinline__ bool job_at(const sdpa_impl::FwdParams& p, int u, int sub, Work& w) {
-  const int P = pairs_per_head(p.n_tiles);
-  const int uph = units_per_head(p.n_tiles);
-  const int bh = u / uph;
-  const int k = u - bh * uph;
+__device__ __forceinline__ bool job_tiles(int n_tiles, int k, int sub, Work& w) {
+  const int P = pairs_per_head(n_tiles);
   const int pr = (sub == 0) ? (P - 1 - k) : k;
   if (sub == 1 && pr == P - 1 - k) return false;
-  w.batch = bh / p.H;
-  w.head = bh - w.batch * p.H;
   w.n_kv_max = 0;
 #pragma unroll
   for (int t = 0; t < kTilesPerCta; ++t) {
     const int qt = 2 * pr + t;
     w.tile[t] = qt;
-    w.n_kv[t] = (qt >= p.n_tiles) ? 0 : ((MODE == sdpa_impl::kMaskCausal) ? qt + 1 : p.n_tiles);
+    w.n_kv[t] = (qt >= n_tiles) ? 0 : ((MODE == sdpa_impl::kMaskCausal) ? qt + 1 : n_tiles);
     w.n_kv_max = max(w.n_kv_max, w.n_kv[t]);
   }
   return true;
 }
 
-// Calls f(work) for every job of this CTA, in order; stops when f returns false.
-template <int MODE, typename F>
+// Packed sequences: a warp-wide cursor over cu_seqlens, 32 sequences per
+// step.  Lane i holds sequence chunk + i (its start and length and the
+// inclusive count of units up to it within the chunk); `before` counts the
+// units of earlier chunks.  Units are numbered sequence by sequence, each
+// sequence's heads in order.  The offsets are used as the running maximum of
+// their values clamped to [0, total], so sequences never overlap and never
+// leave the buffers, whatever the array holds; for valid offsets (0 first,
+// nondecreasing, total last) that is the identity.  All 32 lanes run it.
+struct SeqCursor {
+  int chunk, before, chunk_units;
+  int carry;      // running-maximum offset where this chunk starts
+  int carry_out;  // ... and where it ends
+  int start, len, incl;
+};
+
+__device__ __forceinline__ void cursor_load(const sdpa_impl::FwdParams& p, SeqCursor& c,
+                                            int lane) {
+  const int seq = c.chunk + lane;
+  int e = c.carry;
+  if (seq < p.n_seqs) e = max(e, min(max(__ldg(p.cu_seqlens + seq + 1), 0), p.L));
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, e, off);
+    if (lane >= off) e = max(e, v);
+  }
+  int st = __shfl_up_sync(0xffffffffu, e, 1);
+  if (lane == 0) st = c.carry;
+  c.start = st;
+  c.len = e - st;
+  c.carry_out = __shfl_sync(0xffffffffu, e, 31);
+  int incl = p.H * units_per_head(tiles_of(c.len));
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += v;
+  }
+  c.incl = incl;
+  c.chunk_units = __shfl_sync(0xffffffffu, incl, 31);
+}
+
+// Locates unit u (u only grows between calls).  False when u is past the
+// last unit.
+template <int MODE>
+__device__ __forceinline__ bool cursor_find(const sdpa_impl::FwdParams& p, SeqCursor& c, int lane,
+                                            int u, int& k, int& n_tiles, Work& w) {
+  while (u >= c.before + c.chunk_units) {
+    if (c.chunk + 32 >= p.n_seqs) return false;
+    c.before += c.chunk_units;
+    c.chunk += 32;
+    c.carry = c.carry_out;
+    cursor_load(p, c, lane);
+  }
+  const int rel = u - c.before;
+  const unsigned hit = __ballot_sync(0xffffffffu, rel < c.incl);
+  const int src = __ffs(static_cast<int>(hit)) - 1;
+  const int incl = __shfl_sync(0xffffffffu, c.incl, src);
+  const int len = __shfl_sync(0xffffffffu, c.len, src);
+  const int start = __shfl_sync(0xffffffffu, c.start, src);
+  n_tiles = tiles_of(len);
+  const int uph = units_per_head(n_tiles);
+  const int r = rel - (incl - p.H * uph);  // unit index within this sequence
+  w.batch = 0;
+  w.head = r / uph;
+  k = r - w.head * uph;
+  w.row0 = start;
+  w.len = len;
+  return true;
+}
+
+// Calls f(work) for every job of this CTA, in order; stops when f returns
+// false.  VARLEN: packed sequences described by p.cu_seqlens.
+template <int MODE, bool VARLEN, typename F>
 __device__ __forceinline__ void for_each_job(const sdpa_impl::FwdParams& p, F&& f) {
-  const int n_units = p.B * p.H * units_per_head(p.n_tiles);
-  for (int u = static_cast<int>(blockIdx.x); u < n_units; u += static_cast<int>(gridDim.x)) {
-#pragma unroll 1
-    for (int sub = 0; sub < 2; ++sub) {
+  const int step = static_cast<int>(gridDim.x);
+  if constexpr (!VARLEN) {
+    const int uph = units_per_head(p.n_tiles);
+    const int n_units = p.B * p.H * uph;
+    for (int u = static_cast<int>(blockIdx.x); u < n_units; u += step) {
+      const int bh = u / uph;
       Work w;
-      if (job_at<MODE>(p, u, sub, w) && !f(w)) return;
+      w.batch = bh / p.H;
+      w.head = bh - w.batch * p.H;
+      w.row0 = 0;
+      w.len = p.L;
+#pragma unroll 1
+      for (int sub = 0; sub < 2; ++sub)
+        if (job_tiles<MODE>(p.n_tiles, u - bh * uph, sub, w) && !f(w)) return;
+    }
+  } else {
+    const int lane = static_cast<int>(threadIdx.x & 31);
+    SeqCursor c{0, 0, 0, min(max(__ldg(p.cu_seqlens), 0), p.L), 0, 0, 0, 0};
+    cursor_load(p, c, lane);
+    for (int u = static_cast<int>(blockIdx.x);; u += step) {
+      Work w;
+      int k, n_tiles;
+      if (!cursor_find<MODE>(p, c, lane, u, k, n_tiles, w)) return;
+#pragma unroll 1
+      for (int sub = 0; sub < 2; ++sub)
+        if (job_tiles<MODE>(n_tiles, k, sub, w) && !f(w)) return;
     }
   }
 }
@@ -295,7 +385,7 @@ __device__ __forceinline__ bool softmax_job(const sdpa_impl::FwdParams& p, const
 
   for (int j = 0; j < n; ++j) {
     const int col0 = j * kBlockN;
-    const bool tail = col0 + kBlockN > p.L;
+    const bool tail = col0 + kBlockN > w.len;
     const bool masked_tile = (MODE == sdpa_impl::kMaskExplicit) || tail ||
                              (MODE == sdpa_impl::kMaskCausal && j == qt);
     // Explicit mask: this row's 128 mask bytes for tile j, one bit per key
@@ -303,7 +393,7 @@ __device__ __forceinline__ bool softmax_job(const sdpa_impl::FwdParams& p, const
     // hides behind the score MMA.
     uint32_t mbits[kBlockN / 32];
     if constexpr (MODE == sdpa_impl::kMaskExplicit) {
-      const bool row_ok = row_g < p.L;
+      const bool row_ok = row_g < w.len;
       const uint8_t* mrow = p.mask + static_cast<int64_t>(row_ok ? row_g : 0) * p.L + col0;
       if (p.mask_vec16 && !tail && row_ok) {
         uint4 x[kBlockN / 16];
@@ -330,7 +420,7 @@ __device__ __forceinline__ bool softmax_job(const sdpa_impl::FwdParams& p, const
           uint32_t bits = 0;
           for (int e = 0; e < 32; ++e) {
             const int c = 32 * w32 + e;
-            const bool removed = !row_ok || col0 + c >= p.L || __ldg(mrow + c) != 0;
+            const bool removed = !row_ok || col0 + c >= w.len || __ldg(mrow + c) != 0;
             bits |= (removed ? 1u : 0u) << e;
           }
           mbits[w32] = bits;
@@ -367,7 +457,7 @@ __device__ __forceinline__ bool softmax_job(const sdpa_impl::FwdParams& p, const
 #pragma unroll
         for (int c = 0; c < kBlockN; ++c) {
           const bool removed =
-              (col0 + c >= p.L) || (MODE == sdpa_impl::kMaskCausal && col0 + c > row_g);
+              (col0 + c >= w.len) || (MODE == sdpa_impl::kMaskCausal && col0 + c > row_g);
           s[c] = removed ? mval : s[c];
         }
       }
@@ -486,14 +576,15 @@ __device__ __forceinline__ bool softmax_job(const sdpa_impl::FwdParams& p, const
     ++cnt.o_seen;
     tc_fence_after();
     const float inv_l = (l > 0.0f) ? (1.0f / l) : 0.0f;
-    if (p.lse != nullptr && row_g < p.L) {
+    if (p.lse != nullptr && row_g < w.len) {
       // log(sum_j exp(scale * s_j)) = ln(l) + m_used * ln(2): l sums 2^(x - m_used).
       constexpr float kLn2 = 0.693147180559945309f;
-      p.lse[w.batch * p.lse_sb + w.head * p.lse_sh + static_cast<int64_t>(row_g) * p.lse_sl] =
+      p.lse[w.batch * p.lse_sb + w.head * p.lse_sh +
+            static_cast<int64_t>(w.row0 + row_g) * p.lse_sl] =
           (l > 0.0f) ? (log2f(l) + m_used) * kLn2 : -INFINITY;
     }
     uint16_t* orow = reinterpret_cast<uint16_t*>(p.out) + w.batch * p.o_sb + w.head * p.o_sh +
-                     static_cast<int64_t>(row_g) * p.o_sl;
+                     static_cast<int64_t>(w.row0 + row_g) * p.o_sl;
 #pragma unroll
     for (int c = 0; c < D / 32; ++c) {
       uint32_t o[32];
@@ -504,7 +595,7 @@ __device__ __forceinline__ bool softmax_job(const sdpa_impl::FwdParams& p, const
       for (int e = 0; e < 16; ++e)
         pw[e] = pack2<BF16>(__uint_as_float(o[2 * e]) * inv_l,
                             __uint_as_float(o[2 * e + 1]) * inv_l);
-      if (row_g < p.L) {
+      if (row_g < w.len) {
         uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
 #pragma unroll
         for (int v = 0; v < 4; ++v)
@@ -521,7 +612,7 @@ __device__ __forceinline__ bool softmax_job(const sdpa_impl::FwdParams& p, const
 }
 
 // ------------------------------------------------------------------ kernel
-template <int D, int MODE, bool BF16>
+template <int D, int MODE, bool BF16, bool VARLEN>
 __global__ void __launch_bounds__(kThreads, 1)
     sdpa_fwd_kernel(const __grid_constant__ sdpa_impl::FwdParams p) {
   using Lay = Layout<D>;
@@ -593,7 +684,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // warps 4..7 -> tile A, 8..11 -> tile B; the same jobs as the other roles
     const int t = (warp - 4) >> 2;
     SoftmaxCounters cnt{0, 0};
-    for_each_job<MODE>(p, [&](const Work& w) {
+    for_each_job<MODE, VARLEN>(p, [&](const Work& w) {
       return softmax_job<D, MODE, BF16>(p, w, t, bars, tmem, warp & 3, lane, cnt);
     });
   } else {
@@ -608,7 +699,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Key/value tiles issued so far over all jobs (ring position) and jobs
     // whose Q was loaded; a give-up drains what was issued.
     int g = 0, k_end = 0, v_end = 0, jobs = 0;
-    for_each_job<MODE>(p, [&](const Work& w) -> bool {
+    for_each_job<MODE, VARLEN>(p, [&](const Work& w) -> bool {
       // The previous job's Q must be consumed (all its S products done).
       if (jobs > 0 && !warp_wait_phase(&bars->q_empty, (jobs - 1) & 1, bars, limit, kSiteEmpty))
         return false;
@@ -619,7 +710,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c = 0; c < Lay::kChunks; ++c)
             tma_tile(sQ + t * Lay::kTileBytes + c * Lay::kChunkBytes, &p.tm_q, &bars->q_full,
-                     c * 64, w.tile[t] * kBlockM, w.head, w.batch, p.pos_q);
+                     c * 64, w.row0 + w.tile[t] * kBlockM, w.head, w.batch, p.pos_q);
       }
       ++jobs;
       for (int j = 0; j < w.n_kv_max; ++j, ++g) {
@@ -633,7 +724,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c = 0; c < Lay::kChunks; ++c)
             tma_tile(sK + s * Lay::kTileBytes + c * Lay::kChunkBytes, &p.tm_k, &bars->k_full[s],
-                     c * 64, j * kBlockN, w.head, w.batch, p.pos_k);
+                     c * 64, w.row0 + j * kBlockN, w.head, w.batch, p.pos_k);
         }
         k_end = g + 1;
         const int sv = g % Lay::kVStages;
@@ -646,7 +737,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c = 0; c < Lay::kChunks; ++c)
             tma_tile(sV + sv * Lay::kTileBytes + c * Lay::kChunkBytes, &p.tm_v, &bars->v_full[sv],
-                     c * 64, j * kBlockN, w.head, w.batch, p.pos_v);
+                     c * 64, w.row0 + j * kBlockN, w.head, w.batch, p.pos_v);
         }
         v_end = g + 1;
       }
@@ -710,7 +801,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int g = 0, jobs = 0;
     uint32_t p_seen[kTilesPerCta] = {0, 0}, t_jobs[kTilesPerCta] = {0, 0};
     uint32_t f_seen[kTilesPerCta] = {0, 0};
-    for_each_job<MODE>(p, [&](const Work& w) -> bool {
+    for_each_job<MODE, VARLEN>(p, [&](const Work& w) -> bool {
       if (!warp_wait_phase(&bars->q_full, jobs & 1, bars, limit, kSiteQFull) ||
           !warp_wait_phase(&bars->k_full[g % Lay::kKStages], (g / Lay::kKStages) & 1, bars, limit,
                            kSiteKFull))
@@ -850,9 +941,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D, int MODE, bool BF16>
+template <int D, int MODE, bool BF16, bool VARLEN>
 cudaError_t launch_one(const sdpa_impl::FwdParams& p, int max_ctas, cudaStream_t stream) {
-  auto kern = sdpa_fwd_kernel<D, MODE, BF16>;
+  auto kern = sdpa_fwd_kernel<D, MODE, BF16, VARLEN>;
   constexpr int smem = Layout<D>::kTotal;
   static bool configured = false;  // one attribute call per instantiation
   if (!configured) {
@@ -869,10 +960,12 @@ cudaError_t launch_one(const sdpa_impl::FwdParams& p, int max_ctas, cudaStream_t
   }
   // Persistent grid: one CTA per SM at most, each walking its share of the
   // equal-cost units.
-  const long long n_units =
-      static_cast<long long>(p.B) * p.H * units_per_head(p.n_tiles);
-  const unsigned grid = static_cast<unsigned>(
-      n_units < static_cast<long long>(max_ctas) ? n_units : static_cast<long long>(max_ctas));
+  const long long n_units = VARLEN
+                                ? p.max_units
+                                : static_cast<long long>(p.B) * p.H * units_per_head(p.n_tiles);
+  long long g = n_units < static_cast<long long>(max_ctas) ? n_units : max_ctas;
+  if (g < 1) g = 1;
+  const unsigned grid = static_cast<unsigned>(g);
   // Programmatic dependent launch: this grid's set-up may start while the
   // previous kernel in the stream drains; the kernel waits for it
   // (griddepcontrol.wait) before its first global-memory access.
@@ -892,13 +985,19 @@ cudaError_t launch_one(const sdpa_impl::FwdParams& p, int max_ctas, cudaStream_t
 template <int D, bool BF16>
 cudaError_t launch_mode(const sdpa_impl::FwdParams& p, int mode, int max_ctas,
                         cudaStream_t stream) {
+  if (p.cu_seqlens != nullptr) {  // packed sequences: causal or no mask
+    if (mode == sdpa_impl::kMaskExplicit) return cudaErrorInvalidValue;
+    return mode == sdpa_impl::kMaskCausal
+               ? launch_one<D, sdpa_impl::kMaskCausal, BF16, true>(p, max_ctas, stream)
+               : launch_one<D, sdpa_impl::kMaskNone, BF16, true>(p, max_ctas, stream);
+  }
   switch (mode) {
     case sdpa_impl::kMaskCausal:
-      return launch_one<D, sdpa_impl::kMaskCausal, BF16>(p, max_ctas, stream);
+      return launch_one<D, sdpa_impl::kMaskCausal, BF16, false>(p, max_ctas, stream);
     case sdpa_impl::kMaskExplicit:
-      return launch_one<D, sdpa_impl::kMaskExplicit, BF16>(p, max_ctas, stream);
+      return launch_one<D, sdpa_impl::kMaskExplicit, BF16, false>(p, max_ctas, stream);
     default:
-      return launch_one<D, sdpa_impl::kMaskNone, BF16>(p, max_ctas, stream);
+      return launch_one<D, sdpa_impl::kMaskNone, BF16, false>(p, max_ctas, stream);
   }
 }
 

@@ -18,8 +18,13 @@ struct FwdParams {
   const uint8_t* mask;  // [L, L] row-major bytes, nonzero = removed; null unless mask mode
   float* lse;           // optional [B, H, L] fp32 log-sum-exp per row (element strides below)
   int64_t lse_sb, lse_sh, lse_sl;
-  int B, H, L;
+  int B, H, L;          // packed sequences: B = 1 and L = total rows
   int n_tiles;          // ceil(L / 128)
+  // Packed sequences (null: dense [B, H, L, D]): sequence i is rows
+  // [cu_seqlens[i], cu_seqlens[i+1]) of the L axis, attended on its own.
+  const int* cu_seqlens;
+  int n_seqs;
+  long long max_units;  // upper bound on the number of work units (grid size)
   float scale_log2;     // scale * log2(e)
   int pos_q[3], pos_k[3], pos_v[3];  // tensor-map coordinate slot (1..3) of L, H, B
   int mask_vec16;       // 1: mask rows may be read as 16-byte vectors (L % 16 == 0, aligned)
@@ -29,10 +34,9 @@ struct FwdParams {
 
 enum MaskMode : int { kMaskNone = 0, kMaskCausal = 1, kMaskExplicit = 2 };
 
-// Launches the fused forward kernel for (head_dim, mask mode, dtype) on
-// `stream`.  Returns the CUDA error of the launch.
-// Launches the persistent forward kernel with at most max_ctas CTAs (one per
-// SM: pass the device's SM count).
+// Launches the persistent forward kernel for (head_dim, mask mode, dtype) on
+// `stream` with at most max_ctas CTAs (one per SM: pass the device's SM
+// count).  Returns the CUDA error of the launch.
 cudaError_t launch_forward(const FwdParams& p, int head_dim, int mask_mode, bool bf16,
                            int max_ctas, cudaStream_t stream);
 

@@ -166,3 +166,38 @@ def test_python_wrapper_type_checks(lib):
     z = torch.zeros(1, 2, 8, 64, dtype=torch.float16)
     with pytest.raises(lib.SdpaError):
         lib.sdpa_forward(y, z, y, is_causal=True)
+
+
+def test_varlen_argument_checks(lib):
+    """sdpa_forward_varlen validates on the host before any CUDA call."""
+    import ctypes
+    import torch
+    c = ctypes.CDLL(_build.LIB_PATH)
+    c.sdpa_forward_varlen.restype = ctypes.c_int
+    arr = lambda vals: (ctypes.c_int64 * len(vals))(*vals)
+    total, H, D = 512, 2, 64
+    st = [H * D, D, 1]                       # (token, head, dim)
+    CU = M                                  # any aligned address stands for the offsets
+
+    def call_v(cu=CU, n_seqs=3, max_seqlen=256, strides=st, o=O, lse=0, lse_stride=None,
+               dim=D, causal=1):
+        return c.sdpa_forward_varlen(
+            ctypes.c_void_p(Q), ctypes.c_void_p(K), ctypes.c_void_p(V), ctypes.c_void_p(o),
+            ctypes.c_void_p(lse) if lse else None, 0, ctypes.c_int64(total), ctypes.c_int64(H),
+            ctypes.c_int64(dim), arr(strides), arr(strides), arr(strides), arr(strides),
+            arr(lse_stride) if lse_stride else None, ctypes.c_void_p(cu) if cu else None,
+            ctypes.c_int64(n_seqs), ctypes.c_int64(max_seqlen), causal,
+            ctypes.c_float(float("nan")), None)
+    assert call_v(cu=0) == 1                                  # NULL offsets
+    assert call_v(n_seqs=0) == 3                              # no sequence
+    assert call_v(max_seqlen=0) == 3
+    assert call_v(dim=96) == 3                                # head dim
+    assert call_v(cu=CU + 2) == 5                             # offsets not 4-byte aligned
+    assert call_v(strides=[H * D, D, 2]) == 5                 # dim stride != 1
+    assert call_v(strides=[H * D + 4, D, 1]) == 5             # token stride not 16-byte multiple
+    assert call_v(o=Q + 1024) == 6                            # out overlaps q
+    assert call_v(cu=O + 64) == 6                             # offsets inside out
+    assert call_v(lse=M + 4096, lse_stride=None) == 1         # lse without strides
+    rc = call_v()
+    if not torch.cuda.is_available():
+        assert rc == 7                                        # valid: fails loudly, no fallback
