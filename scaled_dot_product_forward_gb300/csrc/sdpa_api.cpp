@@ -289,6 +289,12 @@ sdpa_status build_params(const void* q, const void* k, const void* v, void* out,
   p.mask_vec16 = (mask && (L % 16) == 0 && (reinterpret_cast<uintptr_t>(mask) & 15u) == 0);
   pr->mode = is_causal ? sdpa_impl::kMaskCausal
                        : (mask ? sdpa_impl::kMaskExplicit : sdpa_impl::kMaskNone);
+  // Job order: when every head's K and V fit in L2 together (here: at most
+  // 48 MB, of the 129 MB), deal jobs by falling cost for balance; beyond
+  // that, keep each head's jobs together for K/V reuse in L2.
+  const double kv_bytes = 2.0 * 2.0 * static_cast<double>(B) * static_cast<double>(H) *
+                          static_cast<double>(L) * static_cast<double>(D);
+  p.snake = kv_bytes <= 48.0 * 1024 * 1024 ? 1 : 0;
   pr->head_dim = static_cast<int>(D);
   return SDPA_OK;
 }

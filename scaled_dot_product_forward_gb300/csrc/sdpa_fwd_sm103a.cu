@@ -201,6 +201,15 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   }
 }
 
+// Bit i (i = 0..3) set when byte i of `word` is nonzero: the bytes' sign
+// bits after a per-byte "!= 0" compare, gathered by one multiply (byte i's
+// bit 8i+7 times 2^(7(3-i)) lands on bit 28+i; every other product term
+// falls on a distinct bit outside 28..31, so nothing carries into them).
+__device__ __forceinline__ uint32_t nonzero_byte_bits(uint32_t word) {
+  const uint32_t m = __vcmpne4(word, 0u) & 0x80808080u;
+  return (m * 0x00204081u) >> 28;
+}
+
 // Work decomposition shared by every role of a CTA.  A job is one pair of
 // adjacent 128-row query tiles of one (sequence, head).  A unit is pair
 // P-1-k followed by pair k of the same head (P pairs per head): under the
@@ -312,26 +321,66 @@ __device__ __forceinline__ bool cursor_find(const sdpa_impl::FwdParams& p, SeqCu
   return true;
 }
 
+// Dense problems: the next job of this CTA (false at the end).  `it` is the
+// CTA's position; one call site per role keeps the roles' code single.
+//  * units (default): unit u = blockIdx.x, +gridDim.x, ...; its two jobs in
+//    turn (sub 0: pair P-1-k, sub 1: pair k);
+//  * snake (small problems whose heads' K and V all fit in L2): jobs in order
+//    of falling cost -- pair P-1 of every head, then pair P-2, ... -- dealt to
+//    the CTAs 0..G-1, then G-1..0, and so on, which balances unequal causal
+//    jobs far better than whole units when there are few jobs per CTA.
+struct DenseIter {
+  int u, sub;  // units
+  int r;       // snake round
+};
+
+template <int MODE>
+__device__ __forceinline__ bool dense_next(const sdpa_impl::FwdParams& p, DenseIter& it, Work& w) {
+  const int G = static_cast<int>(gridDim.x);
+  const int c = static_cast<int>(blockIdx.x);
+  const int BH = p.B * p.H;
+  w.row0 = 0;
+  w.len = p.L;
+  if (p.snake) {
+    const int P = pairs_per_head(p.n_tiles);
+    const int i = it.r * G + ((it.r & 1) ? G - 1 - c : c);
+    if (i >= BH * P) return false;
+    ++it.r;
+    const int cls = i / BH;
+    const int bh = i - cls * BH;
+    w.batch = bh / p.H;
+    w.head = bh - w.batch * p.H;
+    return job_tiles<MODE>(p.n_tiles, cls, 0, w);  // job 0 of unit k is pair P-1-k
+  }
+  const int uph = units_per_head(p.n_tiles);
+  while (it.u < BH * uph) {
+    const int bh = it.u / uph;
+    const int k = it.u - bh * uph;
+    const int sub = it.sub;
+    if (sub == 0) {
+      it.sub = 1;
+    } else {
+      it.sub = 0;
+      it.u += G;
+    }
+    w.batch = bh / p.H;
+    w.head = bh - w.batch * p.H;
+    if (job_tiles<MODE>(p.n_tiles, k, sub, w)) return true;
+  }
+  return false;
+}
+
 // Calls f(work) for every job of this CTA, in order; stops when f returns
 // false.  VARLEN: packed sequences described by p.cu_seqlens.
 template <int MODE, bool VARLEN, typename F>
 __device__ __forceinline__ void for_each_job(const sdpa_impl::FwdParams& p, F&& f) {
-  const int step = static_cast<int>(gridDim.x);
   if constexpr (!VARLEN) {
-    const int uph = units_per_head(p.n_tiles);
-    const int n_units = p.B * p.H * uph;
-    for (int u = static_cast<int>(blockIdx.x); u < n_units; u += step) {
-      const int bh = u / uph;
-      Work w;
-      w.batch = bh / p.H;
-      w.head = bh - w.batch * p.H;
-      w.row0 = 0;
-      w.len = p.L;
-#pragma unroll 1
-      for (int sub = 0; sub < 2; ++sub)
-        if (job_tiles<MODE>(p.n_tiles, u - bh * uph, sub, w) && !f(w)) return;
-    }
+    DenseIter it{static_cast<int>(blockIdx.x), 0, 0};
+    Work w;
+    while (dense_next<MODE>(p, it, w))
+      if (!f(w)) return;
   } else {
+    const int step = static_cast<int>(gridDim.x);
     const int lane = static_cast<int>(threadIdx.x & 31);
     SeqCursor c{0, 0, 0, min(max(__ldg(p.cu_seqlens), 0), p.L), 0, 0, 0, 0};
     cursor_load(p, c, lane);
@@ -386,8 +435,7 @@ __device__ __forceinline__ bool softmax_job(const sdpa_impl::FwdParams& p, const
   for (int j = 0; j < n; ++j) {
     const int col0 = j * kBlockN;
     const bool tail = col0 + kBlockN > w.len;
-    const bool masked_tile = (MODE == sdpa_impl::kMaskExplicit) || tail ||
-                             (MODE == sdpa_impl::kMaskCausal && j == qt);
+    bool masked_tile = tail || (MODE == sdpa_impl::kMaskCausal && j == qt);
     // Explicit mask: this row's 128 mask bytes for tile j, one bit per key
     // (bit set = removed).  Loaded before waiting for S so their latency
     // hides behind the score MMA.
@@ -403,14 +451,12 @@ __device__ __forceinline__ bool softmax_job(const sdpa_impl::FwdParams& p, const
         for (int w32 = 0; w32 < kBlockN / 32; ++w32) {
           uint32_t bits = 0;
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const uint4 xv = x[(32 * w32 + e) >> 4];
-            const int byte_in_v = (32 * w32 + e) & 15;
-            const uint32_t word = (byte_in_v < 4)    ? xv.x
-                                  : (byte_in_v < 8)  ? xv.y
-                                  : (byte_in_v < 12) ? xv.z
-                                                     : xv.w;
-            bits |= (((word >> (8 * (byte_in_v & 3))) & 0xffu) != 0u ? 1u : 0u) << e;
+          for (int q4 = 0; q4 < 8; ++q4) {  // four bytes at a time
+            const int b0 = 32 * w32 + 4 * q4;
+            const uint4 xv = x[b0 >> 4];
+            const int wi = (b0 & 15) >> 2;
+            const uint32_t word = (wi == 0) ? xv.x : (wi == 1) ? xv.y : (wi == 2) ? xv.z : xv.w;
+            bits |= nonzero_byte_bits(word) << (4 * q4);
           }
           mbits[w32] = bits;
         }
@@ -426,6 +472,10 @@ __device__ __forceinline__ bool softmax_job(const sdpa_impl::FwdParams& p, const
           mbits[w32] = bits;
         }
       }
+      // A tile where none of this warp's 32 rows removes a key needs no
+      // per-element select (warp-uniform, so structured masks skip it).
+      masked_tile = masked_tile ||
+                    __any_sync(0xffffffffu, (mbits[0] | mbits[1] | mbits[2] | mbits[3]) != 0u);
     }
     if (!warp_wait_phase(&bars->s_full[t], cnt.s_seen & 1, bars, limit, kSiteSFull)) {
       ok = false;
@@ -960,9 +1010,10 @@ cudaError_t launch_one(const sdpa_impl::FwdParams& p, int max_ctas, cudaStream_t
   }
   // Persistent grid: one CTA per SM at most, each walking its share of the
   // equal-cost units.
-  const long long n_units = VARLEN
-                                ? p.max_units
-                                : static_cast<long long>(p.B) * p.H * units_per_head(p.n_tiles);
+  const long long n_units =
+      VARLEN ? p.max_units
+             : static_cast<long long>(p.B) * p.H *
+                   (p.snake ? pairs_per_head(p.n_tiles) : units_per_head(p.n_tiles));
   long long g = n_units < static_cast<long long>(max_ctas) ? n_units : max_ctas;
   if (g < 1) g = 1;
   const unsigned grid = static_cast<unsigned>(g);

@@ -25,6 +25,7 @@ struct FwdParams {
   const int* cu_seqlens;
   int n_seqs;
   long long max_units;  // upper bound on the number of work units (grid size)
+  int snake;            // dense only: 1 = jobs by falling cost in snake order (small problems)
   float scale_log2;     // scale * log2(e)
   int pos_q[3], pos_k[3], pos_v[3];  // tensor-map coordinate slot (1..3) of L, H, B
   int mask_vec16;       // 1: mask rows may be read as 16-byte vectors (L % 16 == 0, aligned)

@@ -172,3 +172,20 @@ def test_workload_sampled(sdpa_lib, wid):
         full = sdpa_inputs.full_rows(w)
         assert torch.all(got[:, :, full, :] == 0)
         assert torch.isfinite(got.float()).all()
+
+
+@pytest.mark.parametrize("kind", ["window", "blockdiag", "none_removed"])
+def test_structured_masks(sdpa_lib, kind):
+    """Masks with whole tiles free of removed keys (the kernel skips the
+    per-element select there) and whole tiles removed."""
+    L, D = 640, 64
+    q, k, v = sdpa_inputs.custom((1, 2, L, D), dtype=torch.float16, seed=41)
+    i = torch.arange(L)
+    if kind == "window":          # key j allowed when |i - j| < 100
+        mask = (i[:, None] - i[None, :]).abs() >= 100
+    elif kind == "blockdiag":     # documents of 200 rows
+        mask = (i[:, None] // 200) != (i[None, :] // 200)
+    else:
+        mask = torch.zeros(L, L, dtype=torch.bool)
+    out = run(sdpa_lib, q, k, v, mask=mask)
+    check(out.double().cpu().numpy(), oracle.sdpa(q, k, v, mask=mask), kind)
