@@ -210,3 +210,65 @@ def sdpa_varlen(q, k, v, cu_seqlens, is_causal=False, scale=None, return_lse=Fal
             o = r
         out[sl] = o.transpose(1, 0, 2)
     return (out, lse) if return_lse else out
+
+
+def sparse_compact_indices(idx_local, cu_seqlens_q, cu_seqlens_k, is_causal=True):
+    """Index preparation of the sparse top-k path: per-document key positions
+    (``idx_local`` [total_q, topk] int, -1 = hole) become global key rows with
+    the holes removed, as the FlashInfer pull-request page ("FlashInfer,
+    Cake DSA kernel optimization", blog.secrett2633.cloud) describes in its
+    sections 1 and 3: each row keeps its valid entries in their order,
+    rebased by the document's key offset, followed by -1; ``topk_length``
+    counts them.  An entry is valid when 0 <= l < the document's key count
+    and, with ``is_causal``, l <= the query's position in its document.
+    Plain loops (the definition); returns (idx_global, topk_length) int64."""
+    idx_local = np.asarray(idx_local, dtype=np.int64)
+    cu_q = np.asarray(cu_seqlens_q, dtype=np.int64).reshape(-1)
+    cu_k = np.asarray(cu_seqlens_k, dtype=np.int64).reshape(-1)
+    total_q, topk = idx_local.shape
+    out = np.full((total_q, topk), -1, dtype=np.int64)
+    length = np.zeros(total_q, dtype=np.int64)
+    for b in range(len(cu_q) - 1):
+        nk = cu_k[b + 1] - cu_k[b]
+        for i in range(cu_q[b], cu_q[b + 1]):
+            pos = i - cu_q[b]
+            n = 0
+            for t in range(topk):
+                l = idx_local[i, t]
+                if l < 0 or l >= nk or (is_causal and l > pos):
+                    continue
+                out[i, n] = cu_k[b] + l
+                n += 1
+            length[i] = n
+    return out, length
+
+
+def sdpa_sparse(q, k, v, idx, topk_length=None, scale=None, return_lse=False):
+    """Sparse top-k attention, fp64: query row ``i`` (all of its heads)
+    attends to the key rows ``idx[i, :topk_length[i]]`` of one shared key /
+    value head, the DeepSeek sparse attention forward of the FlashInfer
+    pull-request page (``out, lse = fwd(q, kv, idx, topk_length=...)``).
+    q: [total_q, H, D]; k, v: [total_k, D]; idx: [total_q, topk] global rows;
+    topk_length: [total_q] (None: every entry).  A row with no key gives
+    zeros and lse = -inf, as the dense path's safe softmax.  Returns
+    [total_q, H, D] (and lse [total_q, H])."""
+    q, k, v = _as_f64(q), _as_f64(k), _as_f64(v)
+    idx = np.asarray(idx, dtype=np.int64)
+    total_q, H, D = q.shape
+    n = np.full(total_q, idx.shape[1]) if topk_length is None else \
+        np.asarray(topk_length, dtype=np.int64).reshape(-1)
+    s = default_scale(D) if scale is None else float(scale)
+    out = np.zeros((total_q, H, D))
+    lse = np.full((total_q, H), -np.inf)
+    for i in range(total_q):
+        rows = idx[i, :n[i]]
+        if rows.size == 0:
+            continue
+        ks, vs = k[rows], v[rows]                 # gathered keys and values
+        sc = s * (q[i] @ ks.T)                    # [H, n]
+        m = sc.max(axis=1, keepdims=True)
+        e = np.exp(sc - m)
+        tot = e.sum(axis=1, keepdims=True)
+        out[i] = (e / tot) @ vs
+        lse[i] = (m + np.log(tot))[:, 0]
+    return (out, lse) if return_lse else out
