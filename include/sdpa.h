@@ -211,6 +211,59 @@ SDPA_API sdpa_status sdpa_forward_varlen(const void* q, const void* k, const voi
                                          int64_t n_seqs, int64_t max_seqlen, int is_causal,
                                          float scale, void* stream);
 
+/*
+ * sdpa_sparse_forward -- sparse top-k attention: query row i, every head,
+ * attends only to the key rows idx[i, 0 .. len_i) of one key/value head
+ * shared by all query heads, len_i = topk_length[i] clamped to [0, topk]
+ * (topk when topk_length is NULL).  The DeepSeek sparse attention forward
+ * of "FlashInfer, Cake DSA kernel optimization" (blog.secrett2633.cloud):
+ * `out, lse = fwd(q, kv, idx, topk_length=...)` over hole-free index rows
+ * (sections 1 and 3 of that page); pass the same pointer as k and v for one
+ * shared kv tensor.
+ *
+ * q, out     : DEVICE [total_q, H, D] 16-bit of type `dtype`; q_stride and
+ *              o_stride give 2 strides in ELEMENTS (token, head), multiples
+ *              of 8; the D stride is 1.
+ * k, v       : DEVICE [total_k, D]; k_stride, v_stride = row strides in
+ *              ELEMENTS (multiples of 8).  16-byte aligned pointers.
+ * lse        : NULL or DEVICE fp32 [total_q, H] (lse_stride: token, head).
+ * idx        : DEVICE int32 [total_q, topk] (row stride idx_stride >= topk)
+ *              of global key rows; entries outside [0, total_k) inside the
+ *              first len_i are treated as removed keys (no fault).
+ * topk_length: NULL or DEVICE int32 [total_q].
+ * A row with no admissible key gives zeros and lse = -inf.  Computation as
+ * sdpa_forward (16-bit tensor-core products, fp32 softmax).  Errors: NULL,
+ * DTYPE, SHAPE (D not 64/128, an extent < 1), LAYOUT (alignment, strides),
+ * ARG (out or lse overlapping an input, infinite scale), CUDA, DEVICE.
+ * Asynchronous on `stream`; one kernel launch.
+ */
+SDPA_API sdpa_status sdpa_sparse_forward(const void* q, const void* k, const void* v, void* out,
+                                         float* lse, sdpa_dtype dtype, int64_t total_q,
+                                         int64_t total_k, int64_t n_heads, int64_t head_dim,
+                                         const int64_t* q_stride, int64_t k_stride,
+                                         int64_t v_stride, const int64_t* o_stride,
+                                         const int64_t* lse_stride, const int32_t* idx,
+                                         int64_t idx_stride, int64_t topk,
+                                         const int32_t* topk_length, float scale, void* stream);
+
+/*
+ * sdpa_sparse_compact -- the index preparation of the same page (sections 1
+ * and 3) in one launch: per-document key positions become global key rows
+ * with the holes removed.  Query row r of document b (rows
+ * [cu_seqlens_q[b], cu_seqlens_q[b+1])) keeps, in order, every entry l of
+ * idx_local[r, :] with 0 <= l < (cu_seqlens_k[b+1] - cu_seqlens_k[b]) and,
+ * if is_causal, l <= r - cu_seqlens_q[b]; it is written as
+ * cu_seqlens_k[b] + l to idx_global[r, 0 .. n), the rest of the row is -1,
+ * and topk_length[r] = n.  Rows outside every document get n = 0.
+ * All arrays DEVICE int32, 4-byte aligned; offsets nondecreasing.  Errors:
+ * NULL, SHAPE, LAYOUT, ARG (outputs overlapping inputs or each other), CUDA.
+ */
+SDPA_API sdpa_status sdpa_sparse_compact(const int32_t* idx_local, int64_t idx_local_stride,
+                                         int32_t* idx_global, int64_t idx_global_stride,
+                                         int32_t* topk_length, int64_t total_q, int64_t topk,
+                                         const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                                         int64_t n_docs, int is_causal, void* stream);
+
 /* Adds (lse != NULL) or removes (lse == NULL) the log-sum-exp output of a
  * plan; same layout rules as sdpa_forward_lse. */
 SDPA_API sdpa_status sdpa_plan_set_lse(sdpa_plan* plan, float* lse, const int64_t* lse_stride);

@@ -20,7 +20,7 @@ from . import _build
 __all__ = ["sdpa_forward", "sdpa_forward_raw", "sdpa_status_string", "sdpa_last_device_status",
            "sdpa_version", "SdpaError", "load_library", "LIB_PATH", "STATUS",
            "sdpa_debug_set_wait_limit_ns", "sdpa_debug_withhold_q_load", "sdpa_debug_exp2_poly",
-           "sdpa_forward_varlen", "SdpaPlan"]
+           "sdpa_forward_varlen", "sdpa_sparse_forward", "sdpa_sparse_compact", "SdpaPlan"]
 
 LIB_PATH = _build.LIB_PATH
 
@@ -89,6 +89,15 @@ def load_library(path: str | None = None):
                                         i64p, vp, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
                                         ctypes.c_float, vp]
     lib.sdpa_forward_varlen.restype = ctypes.c_int
+    lib.sdpa_sparse_forward.argtypes = [vp, vp, vp, vp, vp, ctypes.c_int, ctypes.c_int64,
+                                        ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, i64p,
+                                        ctypes.c_int64, ctypes.c_int64, i64p, i64p, vp,
+                                        ctypes.c_int64, ctypes.c_int64, vp, ctypes.c_float, vp]
+    lib.sdpa_sparse_forward.restype = ctypes.c_int
+    lib.sdpa_sparse_compact.argtypes = [vp, ctypes.c_int64, vp, ctypes.c_int64, vp,
+                                        ctypes.c_int64, ctypes.c_int64, vp, vp, ctypes.c_int64,
+                                        ctypes.c_int, vp]
+    lib.sdpa_sparse_compact.restype = ctypes.c_int
     if path is None:
         _lib = lib
     return lib
@@ -244,6 +253,86 @@ def sdpa_forward_varlen(q, k, v, cu_seqlens, max_seqlen, out=None, *, is_causal:
     if rc != 0:
         raise SdpaError(rc, "sdpa_forward_varlen")
     return (out, lse) if want_lse else out
+
+
+def sdpa_sparse_forward(q, k, v, idx, topk_length=None, out=None, *, scale=None, stream=None,
+                        return_lse: bool = False, lse=None):
+    """Sparse top-k attention (sdpa_sparse_forward).
+
+    q: [total_q, H, D]; k, v: [total_k, D] (one key/value head shared by all
+    query heads; pass the same tensor twice for one kv tensor); idx: int32
+    [total_q, topk] global key rows; topk_length: optional int32 [total_q].
+    Returns ``out`` [total_q, H, D], or ``(out, lse)`` with lse fp32
+    [total_q, H]."""
+    import torch
+
+    dt = _dtype_code(q)
+    if k.dtype != q.dtype or v.dtype != q.dtype:
+        raise SdpaError(4)
+    if q.dim() != 3 or k.dim() != 2 or v.shape != k.shape or k.shape[1] != q.shape[2]:
+        raise SdpaError(3)
+    if k.stride(1) != 1 or v.stride(1) != 1 or q.stride(2) != 1:
+        raise SdpaError(5)
+    if idx.dtype != torch.int32 or idx.dim() != 2 or idx.shape[0] != q.shape[0] or idx.stride(1) != 1:
+        raise SdpaError(5)
+    if topk_length is not None and (topk_length.dtype != torch.int32 or
+                                    not topk_length.is_contiguous() or
+                                    topk_length.numel() != q.shape[0]):
+        raise SdpaError(5)
+    if out is None:
+        out = torch.empty_like(q, memory_format=torch.contiguous_format)
+    elif out.dtype != q.dtype or out.shape != q.shape:
+        raise SdpaError(3)
+    want_lse = return_lse or lse is not None
+    if want_lse:
+        if lse is None:
+            lse = torch.empty(q.shape[:2], dtype=torch.float32, device=q.device)
+        elif lse.dtype != torch.float32 or tuple(lse.shape) != tuple(q.shape[:2]):
+            raise SdpaError(3)
+    s = float("nan") if scale is None else float(scale)
+    st = (stream if stream is not None else torch.cuda.current_stream(q.device)).cuda_stream
+    rc = load_library().sdpa_sparse_forward(
+        ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k.data_ptr()),
+        ctypes.c_void_p(v.data_ptr()), ctypes.c_void_p(out.data_ptr()),
+        ctypes.c_void_p(lse.data_ptr()) if want_lse else None, dt, q.shape[0], k.shape[0],
+        q.shape[1], q.shape[2], _arr(q.stride()[:2]), k.stride(0), v.stride(0),
+        _arr(out.stride()[:2]), _arr(lse.stride()) if want_lse else None,
+        ctypes.c_void_p(idx.data_ptr()), idx.stride(0), idx.shape[1],
+        ctypes.c_void_p(topk_length.data_ptr()) if topk_length is not None else None,
+        ctypes.c_float(s), ctypes.c_void_p(st) if st else None)
+    if rc != 0:
+        raise SdpaError(rc, "sdpa_sparse_forward")
+    return (out, lse) if want_lse else out
+
+
+def sdpa_sparse_compact(idx_local, cu_seqlens_q, cu_seqlens_k, *, is_causal: bool = True,
+                        stream=None):
+    """Index preparation (sdpa_sparse_compact): per-document key positions
+    ``idx_local`` (int32 [total_q, topk], -1 = hole) -> (global rows with the
+    holes removed and -1 after them, valid counts int32 [total_q])."""
+    import torch
+
+    for t in (idx_local, cu_seqlens_q, cu_seqlens_k):
+        if t.dtype != torch.int32:
+            raise SdpaError(5)
+    if idx_local.dim() != 2 or idx_local.stride(1) != 1:
+        raise SdpaError(5)
+    if not (cu_seqlens_q.is_contiguous() and cu_seqlens_k.is_contiguous()) or \
+            cu_seqlens_q.numel() != cu_seqlens_k.numel():
+        raise SdpaError(3)
+    total_q, topk = idx_local.shape
+    idx_global = torch.empty((total_q, topk), dtype=torch.int32, device=idx_local.device)
+    length = torch.empty(total_q, dtype=torch.int32, device=idx_local.device)
+    st = (stream if stream is not None else torch.cuda.current_stream(idx_local.device)).cuda_stream
+    rc = load_library().sdpa_sparse_compact(
+        ctypes.c_void_p(idx_local.data_ptr()), idx_local.stride(0),
+        ctypes.c_void_p(idx_global.data_ptr()), idx_global.stride(0),
+        ctypes.c_void_p(length.data_ptr()), total_q, topk,
+        ctypes.c_void_p(cu_seqlens_q.data_ptr()), ctypes.c_void_p(cu_seqlens_k.data_ptr()),
+        cu_seqlens_q.numel() - 1, 1 if is_causal else 0, ctypes.c_void_p(st) if st else None)
+    if rc != 0:
+        raise SdpaError(rc, "sdpa_sparse_compact")
+    return idx_global, length
 
 
 def _dtype_code(q):

@@ -324,6 +324,32 @@ ReplaceAddressFn get_replace_fn() {
   return fn;
 }
 
+// A tiled map of `rank` dims (dim 0 contiguous, 16-bit elements) with the
+// given extents, byte strides of dims 1.., and box; 128-byte swizzle, zero
+// fill out of bounds.
+sdpa_status encode_nd(const void* ptr, bool bf16, int rank, const cuuint64_t* gdim,
+                      const cuuint64_t* gstride_bytes, const cuuint32_t* box, CUtensorMap* map) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc) return SDPA_ERR_CUDA;
+  cuuint32_t estride[5] = {1, 1, 1, 1, 1};
+  const CUresult r =
+      enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+          static_cast<cuuint32_t>(rank), const_cast<void*>(ptr), gdim, gstride_bytes, box,
+          estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? SDPA_OK : SDPA_ERR_LAYOUT;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+bool stride_ok(int64_t st) { return st > 0 && (st % 8) == 0; }
+
+// [a, a + bytes) as a span for the overlap checks.
+void span(const void* a, uint64_t bytes, uintptr_t* lo, uintptr_t* hi) {
+  *lo = reinterpret_cast<uintptr_t>(a);
+  *hi = *lo + static_cast<uintptr_t>(bytes);
+}
+
 }  // namespace
 
 struct sdpa_plan {
@@ -431,6 +457,170 @@ sdpa_status sdpa_forward_varlen(const void* q, const void* k, const void* v, voi
   return launch_prepared(pr, stream);
 }
 
+sdpa_status sdpa_sparse_forward(const void* q, const void* k, const void* v, void* out, float* lse,
+                                sdpa_dtype dtype, int64_t total_q, int64_t total_k,
+                                int64_t n_heads, int64_t head_dim, const int64_t* q_stride,
+                                int64_t k_stride, int64_t v_stride, const int64_t* o_stride,
+                                const int64_t* lse_stride, const int32_t* idx, int64_t idx_stride,
+                                int64_t topk, const int32_t* topk_length, float scale,
+                                void* stream) {
+  if (!q || !k || !v || !out || !idx || !q_stride || !o_stride) return SDPA_ERR_NULL;
+  if (lse && !lse_stride) return SDPA_ERR_NULL;
+  if (dtype != SDPA_BF16 && dtype != SDPA_FP16) return SDPA_ERR_DTYPE;
+  if (head_dim != 64 && head_dim != 128) return SDPA_ERR_SHAPE;
+  if (total_q < 1 || total_k < 1 || n_heads < 1 || topk < 1) return SDPA_ERR_SHAPE;
+  const int64_t n_groups = (n_heads + 127) / 128;
+  if (total_k > 0x7fffffffLL || topk > 0x7fffffffLL - 256 || n_heads > 0x7fffffffLL ||
+      total_q > 0x7fffffffLL / n_groups)
+    return SDPA_ERR_SHAPE;
+  // layouts: 16-byte aligned rows (TMA), 4-byte aligned index arrays
+  const int64_t sq_t = q_stride[0], sq_h = (n_heads > 1) ? q_stride[1] : head_dim;
+  const int64_t so_t = o_stride[0], so_h = (n_heads > 1) ? o_stride[1] : head_dim;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return SDPA_ERR_LAYOUT;
+  if ((total_q > 1 && !stride_ok(sq_t)) || !stride_ok(sq_h) || !stride_ok(so_h) ||
+      (total_q > 1 && !stride_ok(so_t)))
+    return SDPA_ERR_LAYOUT;
+  if ((total_k > 1 && (!stride_ok(k_stride) || !stride_ok(v_stride))) || !aligned4(idx) ||
+      (topk_length && !aligned4(topk_length)) || (total_q > 1 && idx_stride < topk))
+    return SDPA_ERR_LAYOUT;
+  if (lse && (!aligned4(lse) || (n_heads > 1 && lse_stride[1] <= 0) ||
+              (total_q > 1 && lse_stride[0] <= 0)))
+    return SDPA_ERR_LAYOUT;
+  if (std::isinf(scale)) return SDPA_ERR_ARG;
+  // out (and lse) must not overlap anything the kernel reads
+  {
+    const uint64_t ob = 2ull * static_cast<uint64_t>((total_q - 1) * so_t + (n_heads - 1) * so_h +
+                                                     head_dim);
+    uintptr_t o0, o1, a0, a1;
+    span(out, ob, &o0, &o1);
+    const void* ins[5] = {q, k, v, idx, topk_length};
+    const uint64_t inb[5] = {
+        2ull * static_cast<uint64_t>((total_q - 1) * sq_t + (n_heads - 1) * sq_h + head_dim),
+        2ull * static_cast<uint64_t>((total_k - 1) * k_stride + head_dim),
+        2ull * static_cast<uint64_t>((total_k - 1) * v_stride + head_dim),
+        4ull * static_cast<uint64_t>((total_q - 1) * idx_stride + topk),
+        4ull * static_cast<uint64_t>(total_q)};
+    for (int t = 0; t < 5; ++t) {
+      if (!ins[t]) continue;
+      span(ins[t], inb[t], &a0, &a1);
+      if (overlaps(o0, o1, a0, a1)) return SDPA_ERR_ARG;
+    }
+    if (lse) {
+      const int64_t lh = (n_heads > 1) ? lse_stride[1] : 0, lt = (total_q > 1) ? lse_stride[0] : 0;
+      uintptr_t l0, l1;
+      span(lse, 4ull * static_cast<uint64_t>((total_q - 1) * lt + (n_heads - 1) * lh + 1), &l0,
+           &l1);
+      if (overlaps(l0, l1, o0, o1)) return SDPA_ERR_ARG;
+      for (int t = 0; t < 5; ++t) {
+        if (!ins[t]) continue;
+        span(ins[t], inb[t], &a0, &a1);
+        if (overlaps(l0, l1, a0, a1)) return SDPA_ERR_ARG;
+      }
+    }
+  }
+  sdpa_status s = check_device();
+  if (s != SDPA_OK) return s;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SDPA_ERR_CUDA;
+  const bool bf16 = (dtype == SDPA_BF16);
+  sdpa_impl::SparseParams p;
+  std::memset(&p, 0, sizeof(p));
+  {
+    // Q: (D, H, total_q); box 64 x 128 heads x 1 row (heads past H read as 0)
+    const cuuint64_t gdim[3] = {static_cast<cuuint64_t>(head_dim),
+                                static_cast<cuuint64_t>(n_heads),
+                                static_cast<cuuint64_t>(total_q)};
+    const cuuint64_t gst[2] = {static_cast<cuuint64_t>(sq_h) * 2u,
+                               static_cast<cuuint64_t>(total_q > 1 ? sq_t : sq_h * n_heads) * 2u};
+    // (with fewer than 128 heads the box is H rows; the tile's other rows
+    // are never stored)
+    p.q_rows = static_cast<int>(n_heads < 128 ? n_heads : 128);
+    const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(p.q_rows), 1};
+    if ((s = encode_nd(q, bf16, 3, gdim, gst, box, &p.tm_q)) != SDPA_OK) return s;
+    // K, V: (D, total_k), one-row boxes for the row gathers
+    const cuuint64_t kd[2] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(total_k)};
+    const cuuint64_t ks[1] = {static_cast<cuuint64_t>(total_k > 1 ? k_stride : head_dim) * 2u};
+    const cuuint64_t vs[1] = {static_cast<cuuint64_t>(total_k > 1 ? v_stride : head_dim) * 2u};
+    const cuuint32_t kb[2] = {64, 1};
+    if ((s = encode_nd(k, bf16, 2, kd, ks, kb, &p.tm_k)) != SDPA_OK) return s;
+    if ((s = encode_nd(v, bf16, 2, kd, vs, kb, &p.tm_v)) != SDPA_OK) return s;
+  }
+  p.out = out;
+  p.o_st = so_t;
+  p.o_sh = so_h;
+  p.lse = lse;
+  if (lse) {
+    p.lse_st = (total_q > 1) ? lse_stride[0] : 0;
+    p.lse_sh = (n_heads > 1) ? lse_stride[1] : 0;
+  }
+  p.idx = idx;
+  p.idx_st = idx_stride;
+  p.topk_length = topk_length;
+  p.total_q = static_cast<int>(total_q);
+  p.total_k = static_cast<int>(total_k);
+  p.H = static_cast<int>(n_heads);
+  p.topk = static_cast<int>(topk);
+  p.n_groups = static_cast<int>(n_groups);
+  const double sc = std::isnan(scale) ? 1.0 / std::sqrt(static_cast<double>(head_dim))
+                                      : static_cast<double>(scale);
+  p.scale_log2 = static_cast<float>(sc * 1.4426950408889634);
+  if (p.scale_log2 == 0.0f) p.scale_log2 = std::signbit(sc) ? -FLT_MIN : FLT_MIN;
+  p.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
+  const int sms = g_device_sms[dev].load(std::memory_order_relaxed);
+  const cudaError_t e = sdpa_impl::launch_sparse(p, static_cast<int>(head_dim), bf16, sms,
+                                                 static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;
+}
+
+sdpa_status sdpa_sparse_compact(const int32_t* idx_local, int64_t idx_local_stride,
+                                int32_t* idx_global, int64_t idx_global_stride,
+                                int32_t* topk_length, int64_t total_q, int64_t topk,
+                                const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                                int64_t n_docs, int is_causal, void* stream) {
+  if (!idx_local || !idx_global || !topk_length || !cu_seqlens_q || !cu_seqlens_k)
+    return SDPA_ERR_NULL;
+  if (total_q < 1 || topk < 1 || n_docs < 1 || total_q > 0x7fffffffLL / 32 ||
+      topk > 0x7fffffffLL - 64 || n_docs > 0x7fffffffLL - 1)
+    return SDPA_ERR_SHAPE;
+  if (!aligned4(idx_local) || !aligned4(idx_global) || !aligned4(topk_length) ||
+      !aligned4(cu_seqlens_q) || !aligned4(cu_seqlens_k) ||
+      (total_q > 1 && (idx_local_stride < topk || idx_global_stride < topk)))
+    return SDPA_ERR_LAYOUT;
+  {
+    // outputs must not overlap inputs or each other
+    uintptr_t g0, g1, n0, n1, a0, a1;
+    span(idx_global, 4ull * static_cast<uint64_t>((total_q - 1) * idx_global_stride + topk), &g0,
+         &g1);
+    span(topk_length, 4ull * static_cast<uint64_t>(total_q), &n0, &n1);
+    if (overlaps(g0, g1, n0, n1)) return SDPA_ERR_ARG;
+    const void* ins[3] = {idx_local, cu_seqlens_q, cu_seqlens_k};
+    const uint64_t inb[3] = {
+        4ull * static_cast<uint64_t>((total_q - 1) * idx_local_stride + topk),
+        4ull * static_cast<uint64_t>(n_docs + 1), 4ull * static_cast<uint64_t>(n_docs + 1)};
+    for (int t = 0; t < 3; ++t) {
+      span(ins[t], inb[t], &a0, &a1);
+      if (overlaps(g0, g1, a0, a1) || overlaps(n0, n1, a0, a1)) return SDPA_ERR_ARG;
+    }
+  }
+  const sdpa_status s = check_device();
+  if (s != SDPA_OK) return s;
+  sdpa_impl::CompactParams p;
+  p.idx_local = idx_local;
+  p.in_st = idx_local_stride;
+  p.idx_global = idx_global;
+  p.out_st = idx_global_stride;
+  p.length = topk_length;
+  p.cu_q = cu_seqlens_q;
+  p.cu_k = cu_seqlens_k;
+  p.total_q = static_cast<int>(total_q);
+  p.topk = static_cast<int>(topk);
+  p.n_docs = static_cast<int>(n_docs);
+  p.is_causal = is_causal ? 1 : 0;
+  return sdpa_impl::launch_compact(p, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? SDPA_OK
+             : SDPA_ERR_CUDA;
+}
+
 sdpa_status sdpa_plan_create(sdpa_plan** plan, const void* q, const void* k, const void* v,
                              void* out, sdpa_dtype dtype, int rank, const int64_t* shape,
                              const int64_t* q_stride, const int64_t* k_stride,
@@ -532,10 +722,12 @@ const char* sdpa_status_string(sdpa_status status) {
 }
 
 sdpa_status sdpa_last_device_status(void* stream, uint32_t* detail) {
-  unsigned int st = 0;
+  unsigned int st = 0, st_sparse = 0;
   if (sdpa_impl::read_and_clear_device_status(static_cast<cudaStream_t>(stream), &st) !=
-      cudaSuccess)
+          cudaSuccess ||
+      sdpa_impl::read_and_clear_sparse_status(&st_sparse) != cudaSuccess)
     return SDPA_ERR_CUDA;
+  st |= st_sparse;
   if (detail) *detail = st;
   return st == 0 ? SDPA_OK : SDPA_ERR_DEVICE_TIMEOUT;
 }

@@ -33,6 +33,43 @@ struct FwdParams {
   uint64_t wait_limit_ns;  // bound on any single barrier wait
 };
 
+// Sparse top-k attention: query row i (all heads of head group g) attends to
+// the key rows idx[i, 0 .. len_i) of one shared key/value head.
+struct SparseParams {
+  CUtensorMap tm_q;  // 3-D (D, H, total_q), box 64 x 128 x 1 (head group of 128)
+  CUtensorMap tm_k;  // 2-D (D, total_k), box 64 x 1 (row gathers)
+  CUtensorMap tm_v;
+  void* out;                // [total_q, H, D]
+  int64_t o_st, o_sh;
+  float* lse;               // optional [total_q, H]
+  int64_t lse_st, lse_sh;
+  const int* idx;           // [total_q, topk] global key rows
+  int64_t idx_st;
+  const int* topk_length;   // [total_q] valid leading entries, or null (all topk)
+  int total_q, total_k, H, topk, n_groups;
+  int q_rows;               // rows of the Q box: min(H, 128)
+  float scale_log2;
+  uint64_t wait_limit_ns;
+};
+
+// Index preparation: per-document key positions -> global rows, holes removed.
+struct CompactParams {
+  const int* idx_local;
+  int64_t in_st;
+  int* idx_global;
+  int64_t out_st;
+  int* length;
+  const int* cu_q;
+  const int* cu_k;
+  int total_q, topk, n_docs, is_causal;
+};
+
+cudaError_t launch_sparse(const SparseParams& p, int head_dim, bool bf16, int max_ctas,
+                          cudaStream_t stream);
+cudaError_t launch_compact(const CompactParams& p, cudaStream_t stream);
+// Reads and clears the sparse kernel's status word (its own translation unit).
+cudaError_t read_and_clear_sparse_status(unsigned int* status);
+
 enum MaskMode : int { kMaskNone = 0, kMaskCausal = 1, kMaskExplicit = 2 };
 
 // Launches the persistent forward kernel for (head_dim, mask mode, dtype) on

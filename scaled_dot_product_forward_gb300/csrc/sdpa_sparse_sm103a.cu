@@ -1,0 +1,634 @@
+// sdpa_sparse_sm103a.cu -- sparse top-k attention forward and its index
+// preparation, for sm_103a.
+//
+// The DeepSeek sparse attention (DSA) forward of "FlashInfer, Cake DSA kernel
+// optimization" (blog.secrett2633.cloud): every query row attends only to the
+// key rows its index row lists, over one key/value head shared by all query
+// heads (`out, lse = fwd(q, kv, idx, topk_length=...)`), and the index rows
+// are hole-free -- the valid entries first, counted by topk_length -- after a
+// single-launch preparation that turns per-document positions into global
+// rows (same page, sections 1 and 3).
+//
+// Forward, built the way the dense kernel is, for one shared key set per query
+// row instead of one per tile:
+//   * a job is one query row and a group of up to 128 of its heads: the heads
+//     are the 128 rows of the tensor-core tile (M = 128; groups of fewer heads
+//     are zero-padded by the tensor map), and they share the gathered keys;
+//   * warp 0 loads the job's Q with a 3-D TMA box and gathers K and V rows by
+//     index with TMA row gathers (four rows per instruction, 128 keys per
+//     stage), after checking every index (entries past the row's count or out
+//     of range become row 0 and are removed in the softmax);
+//   * warp 1 issues S = Q K^T into two alternating TMEM buffers, so S(j+1)
+//     runs while the softmax works on S(j), and O += P V with P in its own
+//     TMEM columns;
+//   * warpgroup 1 runs the online softmax, one head row per thread, as in the
+//     dense kernel, and writes O / l and the log-sum-exp.
+// Every barrier wait is bounded in time; on expiry the CTA records a status
+// bit (read with the dense kernel's by sdpa_last_device_status), stops and
+// frees its tensor memory.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "ptx.cuh"
+#include "sdpa_internal.h"
+
+using namespace sdpa_dev;
+
+__device__ unsigned int g_sdpa_sparse_status = 0;
+
+namespace {
+
+constexpr int kRows = 128;     // head rows per job (TMEM lanes)
+constexpr int kKeys = 128;     // gathered keys per stage
+constexpr int kThreads = 256;  // WG0: TMA, MMA, 2 idle; WG1: softmax
+constexpr float kRescaleLog2 = 8.0f;
+
+template <int D>
+struct SLayout {
+  static constexpr int kChunks = D / 64;
+  static constexpr int kChunkBytes = kKeys * 128;  // 128 rows x 64 elements
+  static constexpr int kTileBytes = kChunks * kChunkBytes;
+  static constexpr int kStages = (D == 64) ? 6 : 3;
+  static constexpr int kMaskSlots = kStages + 2;   // see the softmax
+  static constexpr int kQ = 0;
+  static constexpr int kK = kQ + kTileBytes;
+  static constexpr int kV = kK + kStages * kTileBytes;
+  static constexpr int kBar = kV + kStages * kTileBytes;
+  static constexpr int kBarBytes = 1024;
+  static constexpr int kTotal = kBar + kBarBytes + 1024;
+};
+static_assert(SLayout<128>::kTotal <= 227 * 1024, "shared memory over the per-CTA limit");
+static_assert(SLayout<64>::kTotal <= 227 * 1024, "shared memory over the per-CTA limit");
+
+// TMEM columns: S0 [0,128), S1 [128,256), O [256, 256+D), P [384, 448).
+constexpr uint32_t kColS0 = 0, kColO = 256, kColP = 384, kTmemCols = 512;
+
+constexpr int kMaxStages = 8;
+struct SBarriers {
+  uint64_t q_full, q_empty;
+  uint64_t s_full[2], s_free[2];
+  uint64_t p_ready, o_done, o_free, fin;
+  uint64_t k_full[kMaxStages], k_empty[kMaxStages];
+  uint64_t v_full[kMaxStages], v_empty[kMaxStages];
+  // Validity of the 128 gathered keys of K tile g, in slot g % kMaskSlots:
+  // word e bit l = key 4l + e (one ballot per lane position); m_full[slot]
+  // completes when the producer has written it.
+  uint64_t m_full[kMaxStages + 2];
+  uint32_t kmask[kMaxStages + 2][4];
+  uint32_t tmem_base;
+  uint32_t abort_flag;
+};
+static_assert(sizeof(SBarriers) <= 1024, "barrier block too large");
+
+enum SparseSite : unsigned int {
+  kSpQ = 1u << 1, kSpK = 1u << 2, kSpEmpty = 1u << 3, kSpS = 1u << 4, kSpP = 1u << 5,
+  kSpO = 1u << 6, kSpDrain = 1u << 7, kSpV = 1u << 8, kSpSFree = 1u << 9,
+};
+
+__device__ __forceinline__ bool swait(uint64_t* bar, uint32_t parity, SBarriers* bars,
+                                      uint64_t limit_ns, unsigned int site,
+                                      bool honour_abort = true) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  uint32_t spins = 0;
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((++spins & 63u) == 0) {
+      if (honour_abort && *reinterpret_cast<volatile uint32_t*>(&bars->abort_flag) != 0)
+        return false;
+      if (global_timer_ns() - t0 > limit_ns) {
+        *reinterpret_cast<volatile uint32_t*>(&bars->abort_flag) = 1u;
+        atomicOr(&g_sdpa_sparse_status, 1u | site);
+        return false;
+      }
+    }
+  }
+}
+__device__ __forceinline__ bool warp_swait(uint64_t* bar, uint32_t parity, SBarriers* bars,
+                                           uint64_t limit_ns, unsigned int site) {
+  return __all_sync(0xffffffffu, swait(bar, parity, bars, limit_ns, site));
+}
+
+template <bool BF16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  if constexpr (BF16) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+  } else {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+  }
+}
+
+// A job: query row `row`, heads [128 * group, +128), n_kv key tiles.
+struct SJob {
+  int row, group, len, n_kv;
+};
+
+__device__ __forceinline__ bool job_of(const sdpa_impl::SparseParams& p, int j, SJob& job) {
+  if (j >= p.total_q * p.n_groups) return false;
+  job.row = j / p.n_groups;
+  job.group = j - job.row * p.n_groups;
+  int len = p.topk;
+  if (p.topk_length != nullptr) len = min(max(__ldg(p.topk_length + job.row), 0), p.topk);
+  job.len = len;
+  job.n_kv = (len + kKeys - 1) / kKeys;
+  return true;
+}
+
+template <int D, bool BF16>
+__global__ void __launch_bounds__(kThreads, 1)
+    sparse_fwd_kernel(const __grid_constant__ sdpa_impl::SparseParams p) {
+  using Lay = SLayout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sQ = smem + Lay::kQ;
+  uint8_t* sK = smem + Lay::kK;
+  uint8_t* sV = smem + Lay::kV;
+  SBarriers* bars = reinterpret_cast<SBarriers*>(smem + Lay::kBar);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint64_t limit = p.wait_limit_ns;
+  const int step = static_cast<int>(gridDim.x);
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->q_full, 1);
+    mbar_init(&bars->q_empty, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bars->s_full[b], 1);
+      mbar_init(&bars->s_free[b], kRows / 32);
+    }
+    mbar_init(&bars->p_ready, kRows / 32);
+    mbar_init(&bars->o_done, 1);
+    mbar_init(&bars->o_free, kRows / 32);
+    mbar_init(&bars->fin, 1);
+    for (int s = 0; s < Lay::kMaskSlots; ++s) mbar_init(&bars->m_full[s], 1);
+    for (int s = 0; s < Lay::kStages; ++s) {
+      mbar_init(&bars->k_full[s], 1);
+      mbar_init(&bars->k_empty[s], 1);
+      mbar_init(&bars->v_full[s], 1);
+      mbar_init(&bars->v_empty[s], 1);
+    }
+    bars->abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tensormap(&p.tm_q);
+    prefetch_tensormap(&p.tm_k);
+    prefetch_tensormap(&p.tm_v);
+  }
+  if (warp == 1) {
+    tmem_alloc(&bars->tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  grid_dependency_wait();
+  grid_launch_dependents();
+  const uint32_t tmem = bars->tmem_base;
+
+  if (warp >= 4) {
+    // ---------------------------------------------------- softmax warps
+    const int wq = warp & 3;
+    const int r = wq * 32 + lane;  // head row within the group
+    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+    const float sl2 = p.scale_log2;
+    const bool pos_scale = sl2 >= 0.0f;
+    const float mval = pos_scale ? -INFINITY : INFINITY;
+    uint32_t ns = 0, o_seen = 0;
+    int g = 0;  // K tile counter (mask slot)
+    bool ok = true;
+    SJob job;
+    for (int jj = static_cast<int>(blockIdx.x); ok && job_of(p, jj, job); jj += step) {
+      const int h = job.group * kRows + r;
+      if (job.n_kv == 0) {
+        // no key: zeros and lse = -inf (the safe softmax of an empty row)
+        if (h < p.H) {
+          uint16_t* orow = reinterpret_cast<uint16_t*>(p.out) + job.row * p.o_st + h * p.o_sh;
+          for (int c = 0; c < D; c += 8)
+            *reinterpret_cast<uint4*>(orow + c) = make_uint4(0, 0, 0, 0);
+          if (p.lse != nullptr) p.lse[job.row * p.lse_st + h * p.lse_sh] = -INFINITY;
+        }
+        continue;
+      }
+      float m_used = -INFINITY, l = 0.0f;
+      for (int j = 0; j < job.n_kv; ++j, ++g) {
+        const uint32_t b = ns & 1;
+        if (!warp_swait(&bars->s_full[b], (ns >> 1) & 1, bars, limit, kSpS)) {
+          ok = false;
+          break;
+        }
+        ++ns;
+        tc_fence_after();
+        float s[kKeys];
+        {
+          uint32_t su[kKeys];
+#pragma unroll
+          for (int c = 0; c < kKeys / 32; ++c)
+            tmem_ld32(tmem + kColS0 + b * 128 + lane_off + c * 32, su + c * 32);
+          tmem_ld_wait();
+#pragma unroll
+          for (int c = 0; c < kKeys; ++c) s[c] = __uint_as_float(su[c]);
+        }
+        // The key mask is read before S's buffer is released: the producer
+        // refills this slot only after S of a tile two later has completed,
+        // which needs that release (kMaskSlots = stages + 2), so m_full of
+        // the slot is at most one phase ahead of this wait.
+        uint32_t km[4];
+        if (!warp_swait(&bars->m_full[g % Lay::kMaskSlots], (g / Lay::kMaskSlots) & 1, bars, limit,
+                        kSpK)) {
+          ok = false;
+          break;
+        }
+        {
+          const volatile uint32_t* src = bars->kmask[g % Lay::kMaskSlots];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) km[e] = src[e];
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->s_free[b]);
+        const bool all_valid = (km[0] & km[1] & km[2] & km[3]) == 0xffffffffu;
+        if (!all_valid) {
+#pragma unroll
+          for (int c = 0; c < kKeys; ++c) s[c] = ((km[c & 3] >> (c >> 2)) & 1u) ? s[c] : mval;
+        }
+        // row extremum: eight independent chains of three-input max / min
+        float e8[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) e8[i] = s[i];
+        if (pos_scale) {
+#pragma unroll
+          for (int c = 8; c < kKeys; c += 16)
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              e8[i] = max3f(e8[i], s[c + i], s[c + 8 + i < kKeys ? c + 8 + i : c + i]);
+          e8[0] = max3f(e8[0], e8[1], e8[2]);
+          e8[3] = max3f(e8[3], e8[4], e8[5]);
+          e8[6] = fmaxf(e8[6], e8[7]);
+          e8[0] = max3f(e8[0], e8[3], e8[6]);
+        } else {
+#pragma unroll
+          for (int c = 8; c < kKeys; c += 16)
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              e8[i] = min3f(e8[i], s[c + i], s[c + 8 + i < kKeys ? c + 8 + i : c + i]);
+          e8[0] = min3f(e8[0], e8[1], e8[2]);
+          e8[3] = min3f(e8[3], e8[4], e8[5]);
+          e8[6] = fminf(e8[6], e8[7]);
+          e8[0] = min3f(e8[0], e8[3], e8[6]);
+        }
+        const float ext = e8[0];
+        const float m_tile = (ext == mval) ? -INFINITY : ext * sl2;
+        const bool need = m_tile > m_used + kRescaleLog2;
+        float alpha = 1.0f;
+        if (need) {
+          alpha = ex2(m_used - m_tile);
+          m_used = m_tile;
+          l *= alpha;
+        }
+        const float neg_m = (m_used == -INFINITY) ? 0.0f : -m_used;
+#pragma unroll
+        for (int c = 0; c < kKeys; c += 2) fma2_bcast(s[c], s[c + 1], s[c], s[c + 1], sl2, neg_m);
+#pragma unroll
+        for (int c = 0; c < kKeys; ++c) s[c] = ex2(s[c]);
+        uint32_t pk[kKeys / 2];
+        float rs[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) rs[i] = 0.0f;
+#pragma unroll
+        for (int c = 0; c < kKeys / 2; ++c) {
+          add2_acc(rs[2 * (c & 3)], rs[2 * (c & 3) + 1], s[2 * c], s[2 * c + 1]);
+          pk[c] = pack2<BF16>(s[2 * c], s[2 * c + 1]);
+        }
+        add2_acc(rs[0], rs[1], rs[2], rs[3]);
+        add2_acc(rs[4], rs[5], rs[6], rs[7]);
+        add2_acc(rs[0], rs[1], rs[4], rs[5]);
+        l += rs[0] + rs[1];
+        if (j > 0) {
+          // PV(j-1) must be complete before O is rescaled or P is replaced.
+          // Waited here, in order, before the p_ready arrival below.
+          if (!warp_swait(&bars->o_done, o_seen & 1, bars, limit, kSpO)) {
+            ok = false;
+            break;
+          }
+          ++o_seen;
+          tc_fence_after();
+          if (__any_sync(0xffffffffu, need)) {
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+              uint32_t o[32];
+              tmem_ld32(tmem + kColO + lane_off + c * 32, o);
+              tmem_ld_wait();
+              float* of = reinterpret_cast<float*>(o);
+#pragma unroll
+              for (int e = 0; e < 32; e += 2) mul2_bcast(of[e], of[e + 1], alpha);
+              tmem_st32(tmem + kColO + lane_off + c * 32, o);
+            }
+          }
+        }
+        tmem_st32(tmem + kColP + lane_off, pk);
+        tmem_st32(tmem + kColP + lane_off + 32, pk + 32);
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->p_ready);
+      }
+      if (!ok || !warp_swait(&bars->o_done, o_seen & 1, bars, limit, kSpO)) {
+        ok = false;
+        break;
+      }
+      ++o_seen;
+      tc_fence_after();
+      const float inv_l = (l > 0.0f) ? (1.0f / l) : 0.0f;
+      if (h < p.H && p.lse != nullptr) {
+        constexpr float kLn2 = 0.693147180559945309f;
+        p.lse[job.row * p.lse_st + h * p.lse_sh] = (l > 0.0f) ? (log2f(l) + m_used) * kLn2
+                                                              : -INFINITY;
+      }
+      uint16_t* orow = reinterpret_cast<uint16_t*>(p.out) + job.row * p.o_st + h * p.o_sh;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        tmem_ld32(tmem + kColO + lane_off + c * 32, o);
+        tmem_ld_wait();
+        uint32_t pw[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          pw[e] = pack2<BF16>(__uint_as_float(o[2 * e]) * inv_l,
+                              __uint_as_float(o[2 * e + 1]) * inv_l);
+        if (h < p.H) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+          for (int v = 0; v < 4; ++v)
+            dst[v] = make_uint4(pw[4 * v], pw[4 * v + 1], pw[4 * v + 2], pw[4 * v + 3]);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->o_free);
+    }
+    tc_fence_before();
+  } else if (warp == 0) {
+    // ------------------------------------------------------ loads
+    const bool leader = elect_one();
+    int g = 0, k_end = 0, v_end = 0, jobs = 0;
+    bool ok = true;
+    SJob job;
+    for (int jj = static_cast<int>(blockIdx.x); ok && job_of(p, jj, job); jj += step) {
+      if (job.n_kv == 0) continue;
+      if (jobs > 0 && !warp_swait(&bars->q_empty, (jobs - 1) & 1, bars, limit, kSpEmpty)) break;
+      if (leader) {
+        mbar_arrive_expect_tx(&bars->q_full, Lay::kChunks * p.q_rows * 128);
+#pragma unroll
+        for (int c = 0; c < Lay::kChunks; ++c)
+          tma_load_3d(sQ + c * Lay::kChunkBytes, &p.tm_q, &bars->q_full, c * 64,
+                      job.group * kRows, job.row);
+      }
+      ++jobs;
+      const int* irow = p.idx + static_cast<int64_t>(job.row) * p.idx_st;
+      for (int j = 0; j < job.n_kv; ++j, ++g) {
+        const int s = g % Lay::kStages;
+        const int use = g / Lay::kStages;
+        // Lane l gathers keys 4l .. 4l+3 of this tile; an entry past the
+        // row's count or outside [0, total_k) becomes row 0, removed by the
+        // softmax through the mask.
+        int rr[4];
+        uint32_t ballots[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int t = j * kKeys + 4 * lane + e;
+          int v = -1;
+          if (t < job.len) v = __ldg(irow + t);
+          const bool valid = v >= 0 && v < p.total_k;
+          rr[e] = valid ? v : 0;
+          ballots[e] = __ballot_sync(0xffffffffu, valid);
+        }
+        if (use > 0 && !warp_swait(&bars->k_empty[s], (use - 1) & 1, bars, limit, kSpEmpty)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          volatile uint32_t* dst = bars->kmask[g % Lay::kMaskSlots];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) dst[e] = ballots[e];
+          mbar_arrive(&bars->m_full[g % Lay::kMaskSlots]);  // release: the mask is written
+        }
+        __syncwarp();
+        if (leader) mbar_arrive_expect_tx(&bars->k_full[s], Lay::kTileBytes);
+        __syncwarp();
+#pragma unroll
+        for (int c = 0; c < Lay::kChunks; ++c)
+          tma_gather4_2d(sK + s * Lay::kTileBytes + c * Lay::kChunkBytes + 4 * lane * 128,
+                         &p.tm_k, &bars->k_full[s], c * 64, rr[0], rr[1], rr[2], rr[3]);
+        k_end = g + 1;
+        if (use > 0 && !warp_swait(&bars->v_empty[s], (use - 1) & 1, bars, limit, kSpEmpty)) {
+          ok = false;
+          break;
+        }
+        if (leader) mbar_arrive_expect_tx(&bars->v_full[s], Lay::kTileBytes);
+        __syncwarp();
+#pragma unroll
+        for (int c = 0; c < Lay::kChunks; ++c)
+          tma_gather4_2d(sV + s * Lay::kTileBytes + c * Lay::kChunkBytes + 4 * lane * 128,
+                         &p.tm_v, &bars->v_full[s], c * 64, rr[0], rr[1], rr[2], rr[3]);
+        v_end = g + 1;
+      }
+    }
+    for (int j = max(0, k_end - Lay::kStages); j < k_end; ++j)
+      swait(&bars->k_full[j % Lay::kStages], (j / Lay::kStages) & 1, bars, limit, kSpDrain,
+            false);
+    for (int j = max(0, v_end - Lay::kStages); j < v_end; ++j)
+      swait(&bars->v_full[j % Lay::kStages], (j / Lay::kStages) & 1, bars, limit, kSpDrain,
+            false);
+    if (jobs > 0) swait(&bars->q_full, (jobs - 1) & 1, bars, limit, kSpDrain, false);
+  } else if (warp == 1) {
+    // ------------------------------------------------------ MMA issue
+    constexpr uint32_t idS = idesc_f16_f32acc(BF16, false, kRows, kKeys);
+    constexpr uint32_t idPV = idesc_f16_f32acc(BF16, true, kRows, D);
+    constexpr uint32_t kHi = desc_hi_sw128(1024);
+    const uint32_t q_lo = desc_lo_sw128(smem_addr(sQ), 16);
+    const uint32_t k_lo = desc_lo_sw128(smem_addr(sK), 16);
+    const uint32_t v_lo = desc_lo_sw128(smem_addr(sV), Lay::kChunkBytes);
+    bool issued_any = false;
+    auto issue_s = [&](uint32_t buf, int s) {
+      const uint32_t b0 = k_lo + static_cast<uint32_t>(s * (Lay::kTileBytes >> 4));
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = ((kk >> 2) * Lay::kChunkBytes + (kk & 3) * 32) >> 4;
+        mma_ss_elect<kHi, kHi>(tmem + kColS0 + buf * 128, q_lo + off, b0 + off, idS,
+                               kk > 0 ? 1u : 0u);
+      }
+      mma_commit_elect(&bars->s_full[buf]);
+    };
+    auto issue_pv = [&](int s, bool accumulate) {
+      const uint32_t b0 = v_lo + static_cast<uint32_t>(s * (Lay::kTileBytes >> 4));
+#pragma unroll
+      for (int kk = 0; kk < kKeys / 16; ++kk)
+        mma_ts_elect<kHi>(tmem + kColO, tmem + kColP + kk * 8, b0 + ((kk * 16 * 128) >> 4), idPV,
+                          (accumulate || kk > 0) ? 1u : 0u);
+      mma_commit_elect(&bars->o_done);
+    };
+    int g = 0, jobs = 0;
+    uint32_t ns = 0, p_seen = 0;
+    bool ok = true;
+    SJob job;
+    // S into the buffer of S(ns); its previous contents (S(ns-2)) must be in
+    // the softmax's registers.
+    auto s_next = [&](int s) -> bool {
+      const uint32_t buf = ns & 1;
+      if (ns >= 2 && !warp_swait(&bars->s_free[buf], ((ns >> 1) - 1) & 1, bars, limit, kSpSFree))
+        return false;
+      tc_fence_after();
+      issue_s(buf, s);
+      mma_commit_elect(&bars->k_empty[s]);
+      ++ns;
+      return true;
+    };
+    for (int jj = static_cast<int>(blockIdx.x); ok && job_of(p, jj, job); jj += step) {
+      if (job.n_kv == 0) continue;
+      if (!warp_swait(&bars->q_full, jobs & 1, bars, limit, kSpQ) ||
+          !warp_swait(&bars->k_full[g % Lay::kStages], (g / Lay::kStages) & 1, bars, limit, kSpK) ||
+          !s_next(g % Lay::kStages))
+        break;
+      issued_any = true;
+      if (job.n_kv == 1) mma_commit_elect(&bars->q_empty);
+      for (int j = 0; j < job.n_kv; ++j) {
+        const int gj = g + j;
+        if (j + 1 < job.n_kv) {
+          const int s1 = (gj + 1) % Lay::kStages;
+          if (!warp_swait(&bars->k_full[s1], ((gj + 1) / Lay::kStages) & 1, bars, limit, kSpK) ||
+              !s_next(s1)) {
+            ok = false;
+            break;
+          }
+          if (j + 2 == job.n_kv) mma_commit_elect(&bars->q_empty);
+        }
+        const int s = gj % Lay::kStages;
+        if (!warp_swait(&bars->v_full[s], (gj / Lay::kStages) & 1, bars, limit, kSpV) ||
+            !warp_swait(&bars->p_ready, p_seen & 1, bars, limit, kSpP)) {
+          ok = false;
+          break;
+        }
+        ++p_seen;
+        // The job's first product overwrites O: the previous epilogue must
+        // have read it.
+        if (j == 0 && jobs > 0 &&
+            !warp_swait(&bars->o_free, (jobs - 1) & 1, bars, limit, kSpO)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        issue_pv(s, j > 0);
+        mma_commit_elect(&bars->v_empty[s]);
+      }
+      g += job.n_kv;
+      ++jobs;
+    }
+    if (issued_any) {
+      mma_commit_elect(&bars->fin);
+      swait(&bars->fin, 0, bars, limit, kSpDrain, false);
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// Index preparation: one warp per query row.
+__global__ void __launch_bounds__(256) compact_kernel(const sdpa_impl::CompactParams p) {
+  const int row = static_cast<int>((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= p.total_q) return;
+  // Document of this row: the last b with cu_q[b] <= row (offsets assumed
+  // nondecreasing; a row outside every document keeps no entry).
+  int lo = 0, hi = p.n_docs;  // answer in [0, n_docs)
+  while (lo + 1 < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(p.cu_q + mid) <= row) lo = mid; else hi = mid;
+  }
+  const int q0 = __ldg(p.cu_q + lo), q1 = __ldg(p.cu_q + lo + 1);
+  const bool inside = row >= q0 && row < q1;
+  const int pos = row - q0;
+  const int k0 = __ldg(p.cu_k + lo);
+  const int nk = __ldg(p.cu_k + lo + 1) - k0;
+  const int* in = p.idx_local + static_cast<int64_t>(row) * p.in_st;
+  int* out = p.idx_global + static_cast<int64_t>(row) * p.out_st;
+  int n = 0;
+  for (int t0 = 0; t0 < p.topk; t0 += 32) {
+    const int t = t0 + lane;
+    const int l = (t < p.topk && inside) ? __ldg(in + t) : -1;
+    const bool valid = l >= 0 && l < nk && (!p.is_causal || l <= pos);
+    const unsigned bal = __ballot_sync(0xffffffffu, valid);
+    if (valid) out[n + __popc(bal & ((1u << lane) - 1u))] = k0 + l;
+    n += __popc(bal);
+  }
+  for (int t = n + lane; t < p.topk; t += 32) out[t] = -1;
+  if (lane == 0) p.length[row] = n;
+}
+
+template <int D, bool BF16>
+cudaError_t launch_sparse_one(const sdpa_impl::SparseParams& p, int max_ctas,
+                              cudaStream_t stream) {
+  auto kern = sparse_fwd_kernel<D, BF16>;
+  constexpr int smem = SLayout<D>::kTotal;
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  const long long jobs = static_cast<long long>(p.total_q) * p.n_groups;
+  const unsigned grid = static_cast<unsigned>(jobs < max_ctas ? jobs : max_ctas);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid > 0 ? grid : 1);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
+}  // namespace
+
+namespace sdpa_impl {
+
+cudaError_t launch_sparse(const SparseParams& p, int head_dim, bool bf16, int max_ctas,
+                          cudaStream_t stream) {
+  if (max_ctas < 1) return cudaErrorInvalidValue;
+  if (head_dim == 64)
+    return bf16 ? launch_sparse_one<64, true>(p, max_ctas, stream)
+                : launch_sparse_one<64, false>(p, max_ctas, stream);
+  return bf16 ? launch_sparse_one<128, true>(p, max_ctas, stream)
+              : launch_sparse_one<128, false>(p, max_ctas, stream);
+}
+
+cudaError_t launch_compact(const CompactParams& p, cudaStream_t stream) {
+  if (p.total_q <= 0) return cudaSuccess;
+  const long long threads = static_cast<long long>(p.total_q) * 32;
+  const unsigned blocks = static_cast<unsigned>((threads + 255) / 256);
+  compact_kernel<<<blocks, 256, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t read_and_clear_sparse_status(unsigned int* status) {
+  cudaError_t e = cudaMemcpyFromSymbol(status, g_sdpa_sparse_status, sizeof(unsigned int));
+  if (e != cudaSuccess) return e;
+  if (*status != 0) {
+    const unsigned int zero = 0;
+    e = cudaMemcpyToSymbol(g_sdpa_sparse_status, &zero, sizeof(unsigned int));
+  }
+  return e;
+}
+
+}  // namespace sdpa_impl

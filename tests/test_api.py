@@ -201,3 +201,51 @@ def test_varlen_argument_checks(lib):
     rc = call_v()
     if not torch.cuda.is_available():
         assert rc == 7                                        # valid: fails loudly, no fallback
+
+
+def test_sparse_argument_checks(lib):
+    """sdpa_sparse_forward and sdpa_sparse_compact validate on the host."""
+    import ctypes
+    import torch
+    c = ctypes.CDLL(_build.LIB_PATH)
+    c.sdpa_sparse_forward.restype = ctypes.c_int
+    c.sdpa_sparse_compact.restype = ctypes.c_int
+    arr = lambda vals: (ctypes.c_int64 * len(vals))(*vals)
+    total_q, total_k, H, D, topk = 64, 512, 16, 128, 128
+    IDX = M
+
+    def fwd(q=Q, o=O, idx=IDX, dim=D, qs=(H * D, D), ks=D, topk_=topk, idx_st=topk, lse=0,
+            lse_stride=None):
+        return c.sdpa_sparse_forward(
+            ctypes.c_void_p(q), ctypes.c_void_p(K), ctypes.c_void_p(V), ctypes.c_void_p(o),
+            ctypes.c_void_p(lse) if lse else None, 0, ctypes.c_int64(total_q),
+            ctypes.c_int64(total_k), ctypes.c_int64(H), ctypes.c_int64(dim), arr(qs),
+            ctypes.c_int64(ks), ctypes.c_int64(D), arr((H * D, D)),
+            arr(lse_stride) if lse_stride else None, ctypes.c_void_p(idx) if idx else None,
+            ctypes.c_int64(idx_st), ctypes.c_int64(topk_), None, ctypes.c_float(float("nan")),
+            None)
+    assert fwd(idx=0) == 1                       # NULL index array
+    assert fwd(lse=M + 65536) == 1               # lse without strides
+    assert fwd(dim=96) == 3
+    assert fwd(topk_=0) == 3
+    assert fwd(q=Q + 8) == 5                     # q not 16-byte aligned
+    assert fwd(qs=(H * D + 4, D)) == 5           # token stride not a multiple of 8
+    assert fwd(ks=D + 2) == 5
+    assert fwd(idx=IDX + 2) == 5                 # index array not 4-byte aligned
+    assert fwd(idx_st=topk - 1) == 5
+    assert fwd(o=Q + 256) == 6                   # out overlaps q
+    rc = fwd()
+    if not torch.cuda.is_available():
+        assert rc == 7
+
+    def compact(g=O, n=O + (1 << 20), cu_q=M, cu_k=M + 4096, n_docs=2, stride_in=topk):
+        return c.sdpa_sparse_compact(
+            ctypes.c_void_p(IDX + (1 << 22)), ctypes.c_int64(stride_in), ctypes.c_void_p(g),
+            ctypes.c_int64(topk), ctypes.c_void_p(n), ctypes.c_int64(total_q),
+            ctypes.c_int64(topk), ctypes.c_void_p(cu_q) if cu_q else None, ctypes.c_void_p(cu_k),
+            ctypes.c_int64(n_docs), 1, None)
+    assert compact(cu_q=0) == 1
+    assert compact(n_docs=0) == 3
+    assert compact(stride_in=topk - 1) == 5
+    assert compact(g=O + 2) == 5
+    assert compact(n=O + 64) == 6                # lengths overlap the global rows
