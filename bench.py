@@ -315,6 +315,127 @@ def gpu_leg(args, w, rank, world):
                 h2d=h2d, d2h=d2h, flops=flops, host_us=host_us)
 
 
+def extra_leg(args, path):
+    """Packed documents (``--path varlen``) or sparse top-k (``--path
+    sparse``): W warm-up launches, then K launches each timed alone with CUDA
+    events on the launch stream, the 256 MB L2-flush write between them
+    outside the timed pair; e2e through pinned host buffers."""
+    import numpy as np
+    import torch
+
+    import oracle
+    import scaled_dot_product_forward_gb300 as sdpa
+    import sdpa_inputs
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    sdpa.load_library()
+    stream = torch.cuda.Stream(dev)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    if path == "varlen":
+        cfgd = sdpa_inputs.VARLEN_DOCS
+        q, k, v, cu, lengths = sdpa_inputs.make_varlen(**cfgd)
+        H, D = cfgd["H"], cfgd["D"]
+        flops = float(sum(2.0 * H * n * n * D for n in lengths))   # causal convention
+        metric = (f"packed-document causal SDPA fwd TFLOP/s ({cfgd['n_docs']} documents of "
+                  f"{cfgd['lo']}-{cfgd['hi']} tokens, H{H} D{D} bf16)")
+        config = {"workload": "packed causal documents", "n_docs": cfgd["n_docs"],
+                  "lengths": lengths, "total": int(cu[-1]), "H": H, "D": D,
+                  "launch": "sdpa_forward_varlen per step", "l2": "flushed between launches"}
+        ins = [q, k, v, cu]
+        maxlen = max(lengths)
+
+        def launch(t, out):
+            sdpa.sdpa_forward_varlen(t[0], t[1], t[2], t[3], maxlen, out, is_causal=True,
+                                     stream=stream)
+    else:
+        cfgd = sdpa_inputs.SPARSE_DSA
+        q, kv, idx, length = sdpa_inputs.make_sparse(**cfgd)
+        H, D = cfgd["H"], cfgd["D"]
+        flops = 4.0 * H * D * float(length.sum())
+        metric = (f"sparse top-k SDPA fwd TFLOP/s ({cfgd['total']} tokens, H{H} D{D}, "
+                  f"top-{cfgd['topk']} causal index rows, one shared KV head, bf16)")
+        config = {"workload": "sparse top-k (DSA-style)", "total": cfgd["total"], "H": H,
+                  "D": D, "topk": cfgd["topk"], "index_rows": "causal, hole-free",
+                  "kv": "one tensor as key and value (fwd(q, kv, idx))",
+                  "launch": "sdpa_sparse_forward per step", "l2": "flushed between launches"}
+        ins = [q, kv, idx, length]
+
+        def launch(t, out):
+            sdpa.sdpa_sparse_forward(t[0], t[1], t[1], t[2], t[3], out, stream=stream)
+    dins = [x.to(dev) for x in ins]
+    out = torch.empty_like(dins[0])
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            launch(dins, out)
+    stream.synchronize()
+    rc, detail = sdpa.sdpa_last_device_status(stream)
+    if rc != 0:
+        raise RuntimeError(f"warm-up reported {sdpa.sdpa_status_string(rc)} ({detail:#x})")
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    evs = []
+    with torch.cuda.stream(stream):
+        for _ in range(args.steps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            launch(dins, out)
+            e1.record(stream)
+            evs.append((e0, e1))
+    stream.synchronize()
+    clk = clocks.stop()
+    per = [a.elapsed_time(b) for a, b in evs]
+    ms = statistics.fmean(per)
+    # e2e: pinned host inputs in, output back, every step
+    hins = [x.pin_memory() for x in ins]
+    hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    with torch.cuda.stream(stream):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.e2e_steps):
+            for d, h in zip(dins, hins):
+                d.copy_(h, non_blocking=True)
+            launch(dins, out)
+            hout.copy_(out, non_blocking=True)
+        e1.record(stream)
+    stream.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
+    peak, _, peak_kind = load_peaks()
+    achieved = flops / (ms * 1e-3) / 1e12
+    line = {"metric": metric, "value": achieved, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": config,
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
+                         "frac": achieved / peak, "peak_source": f"{peak_kind} dense bf16 (burst)",
+                         "traffic": None, "alg_flops_per_launch": flops, "mean_launch_ms": ms},
+            "e2e": {"value": flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+                    "h2d_bytes_per_step": sum(x.numel() * x.element_size() for x in ins),
+                    "d2h_bytes_per_step": out.numel() * out.element_size(),
+                    "ms_per_step": e2e_ms},
+            "gpu_launches": args.steps, "clocks": clk}
+    if not args.no_cpu_baseline:
+        # the oracle on a bounded sample: one document / a few query rows
+        t0 = time.perf_counter()
+        if path == "varlen":
+            n = min(lengths)
+            oracle.sdpa_varlen(q[:n, :1], k[:n, :1], v[:n, :1], [0, n], is_causal=True)
+            f = 2.0 * 1 * n * n * D
+            sample = f"one head of one {n}-token document"
+        else:
+            rows = 64
+            sel = torch.arange(q.shape[0] - rows, q.shape[0])
+            oracle.sdpa_sparse(q[sel], kv, kv, idx[sel].numpy(), topk_length=length[sel].numpy())
+            f = 4.0 * H * D * float(length[sel].sum())
+            sample = f"the last {rows} query rows (all heads)"
+        t = time.perf_counter() - t0
+        line["cpu_baseline"] = {"value": f / t / 1e12, "unit": UNIT,
+                                "cores": oracle.num_threads(), "kind": "oracle",
+                                "sample": f"{sample}, {t:.1f} s"}
+    return line
+
+
 def max_over_ranks(x: float, world: int) -> float:
     if world <= 1:
         return x
@@ -338,9 +459,16 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--graph", action="store_true",
                     help="time a CUDA graph of K plan launches (no host gaps between kernels)")
+    ap.add_argument("--path", choices=["dense", "varlen", "sparse"], default="dense",
+                    help="dense (the default contract line), packed documents or sparse top-k")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.path != "dense":
+        if args.impl == "reference" or int(os.environ.get("WORLD_SIZE", "1")) > 1:
+            ap.error("--path varlen/sparse measures one GPU with the fused kernels only")
+        print(json.dumps(extra_leg(args, args.path)))
+        return 0
 
     import sdpa_inputs
     w = sdpa_inputs.WORKLOADS[args.workload]

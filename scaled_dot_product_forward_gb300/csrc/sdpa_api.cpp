@@ -553,6 +553,7 @@ sdpa_status sdpa_sparse_forward(const void* q, const void* k, const void* v, voi
     p.lse_st = (total_q > 1) ? lse_stride[0] : 0;
     p.lse_sh = (n_heads > 1) ? lse_stride[1] : 0;
   }
+  p.kv_shared = (k == v && (total_k == 1 || k_stride == v_stride)) ? 1 : 0;
   p.idx = idx;
   p.idx_st = idx_stride;
   p.topk_length = topk_length;

@@ -48,6 +48,7 @@ struct SparseParams {
   const int* topk_length;   // [total_q] valid leading entries, or null (all topk)
   int total_q, total_k, H, topk, n_groups;
   int q_rows;               // rows of the Q box: min(H, 128)
+  int kv_shared;            // 1: k and v are one tensor (gather once, use twice)
   float scale_log2;
   uint64_t wait_limit_ns;
 };

@@ -389,23 +389,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       ++jobs;
       const int* irow = p.idx + static_cast<int64_t>(job.row) * p.idx_st;
+      // Lane l gathers keys 4l .. 4l+3 of a tile.  The indices of tile j+1
+      // are loaded while tile j's rows are requested, so the index load's
+      // latency is off the path.
+      int nxt[4];
+      auto load_idx = [&](int j, int (&dst)[4]) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int t = j * kKeys + 4 * lane + e;
+          dst[e] = (t < job.len) ? __ldg(irow + t) : -1;
+        }
+      };
+      load_idx(0, nxt);
       for (int j = 0; j < job.n_kv; ++j, ++g) {
         const int s = g % Lay::kStages;
         const int use = g / Lay::kStages;
-        // Lane l gathers keys 4l .. 4l+3 of this tile; an entry past the
-        // row's count or outside [0, total_k) becomes row 0, removed by the
-        // softmax through the mask.
+        // An entry past the row's count or outside [0, total_k) becomes row
+        // 0, removed by the softmax through the mask.
         int rr[4];
         uint32_t ballots[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const int t = j * kKeys + 4 * lane + e;
-          int v = -1;
-          if (t < job.len) v = __ldg(irow + t);
+          const int v = nxt[e];
           const bool valid = v >= 0 && v < p.total_k;
           rr[e] = valid ? v : 0;
           ballots[e] = __ballot_sync(0xffffffffu, valid);
         }
+        if (j + 1 < job.n_kv) load_idx(j + 1, nxt);
         if (use > 0 && !warp_swait(&bars->k_empty[s], (use - 1) & 1, bars, limit, kSpEmpty)) {
           ok = false;
           break;
@@ -424,6 +434,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_gather4_2d(sK + s * Lay::kTileBytes + c * Lay::kChunkBytes + 4 * lane * 128,
                          &p.tm_k, &bars->k_full[s], c * 64, rr[0], rr[1], rr[2], rr[3]);
         k_end = g + 1;
+        if (p.kv_shared) {
+          // one kv tensor: the K rows just gathered are the V rows too
+          if (leader) mbar_arrive(&bars->v_full[s]);
+          __syncwarp();
+          continue;
+        }
         if (use > 0 && !warp_swait(&bars->v_empty[s], (use - 1) & 1, bars, limit, kSpEmpty)) {
           ok = false;
           break;
@@ -451,7 +467,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr uint32_t kHi = desc_hi_sw128(1024);
     const uint32_t q_lo = desc_lo_sw128(smem_addr(sQ), 16);
     const uint32_t k_lo = desc_lo_sw128(smem_addr(sK), 16);
-    const uint32_t v_lo = desc_lo_sw128(smem_addr(sV), Lay::kChunkBytes);
+    // V rows: their own stages, or the K stage when one kv tensor serves both
+    const uint32_t v_lo = desc_lo_sw128(smem_addr(p.kv_shared ? sK : sV), Lay::kChunkBytes);
     bool issued_any = false;
     auto issue_s = [&](uint32_t buf, int s) {
       const uint32_t b0 = k_lo + static_cast<uint32_t>(s * (Lay::kTileBytes >> 4));
@@ -483,7 +500,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         return false;
       tc_fence_after();
       issue_s(buf, s);
-      mma_commit_elect(&bars->k_empty[s]);
+      if (!p.kv_shared) mma_commit_elect(&bars->k_empty[s]);  // else after PV
       ++ns;
       return true;
     };
@@ -522,7 +539,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
         issue_pv(s, j > 0);
-        mma_commit_elect(&bars->v_empty[s]);
+        mma_commit_elect(p.kv_shared ? &bars->k_empty[s] : &bars->v_empty[s]);
       }
       g += job.n_kv;
       ++jobs;

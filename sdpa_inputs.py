@@ -161,3 +161,59 @@ def sample_rows(B: int, H: int, L: int, n: int, seed: int) -> torch.Tensor:
         picks.append((b, h, i))
     uniq = sorted(set(picks))
     return torch.tensor(uniq, dtype=torch.int64)
+
+
+# ---------------------------------------------------------------- packed documents
+VARLEN_DOCS = dict(n_docs=16, lo=512, hi=4096, step=64, H=32, D=128, seed=6000)
+
+
+def varlen_lengths(n_docs: int, lo: int, hi: int, step: int, seed: int) -> list[int]:
+    """Document lengths drawn uniformly from {lo, lo + step, ..., hi}."""
+    g = _gen(seed)
+    k = torch.randint(0, (hi - lo) // step + 1, (n_docs,), generator=g)
+    return [lo + step * int(x) for x in k]
+
+
+def make_varlen(n_docs=16, lo=512, hi=4096, step=64, H=32, D=128, seed=6000,
+                dtype=torch.bfloat16, amplitude=0.5):
+    """Packed [total, H, D] q, k, v of seeded lengths and their int32 offsets."""
+    lengths = varlen_lengths(n_docs, lo, hi, step, seed)
+    total = sum(lengths)
+    q = normal((total, H, D), dtype, seed + 1, amplitude)
+    k = normal((total, H, D), dtype, seed + 2, amplitude)
+    v = normal((total, H, D), dtype, seed + 3, amplitude)
+    cu = torch.zeros(n_docs + 1, dtype=torch.int32)
+    cu[1:] = torch.cumsum(torch.tensor(lengths), 0).to(torch.int32)
+    return q, k, v, cu, lengths
+
+
+# ---------------------------------------------------------------- sparse top-k
+SPARSE_DSA = dict(total=8192, H=64, D=128, topk=2048, seed=7000)
+
+
+def causal_topk_indices(total: int, topk: int, seed: int):
+    """Hole-free index rows of one causal document: row i lists min(i + 1,
+    topk) distinct key rows <= i in random order, then -1; and the counts."""
+    g = _gen(seed)
+    idx = torch.full((total, topk), -1, dtype=torch.int32)
+    length = torch.empty(total, dtype=torch.int32)
+    for i in range(total):
+        n = min(i + 1, topk)
+        if i + 1 <= topk:
+            rows = torch.randperm(i + 1, generator=g)
+        else:
+            rows = torch.randperm(i + 1, generator=g)[:topk]
+        idx[i, :n] = rows.to(torch.int32)
+        length[i] = n
+    return idx, length
+
+
+def make_sparse(total=8192, H=64, D=128, topk=2048, seed=7000, dtype=torch.bfloat16,
+                amplitude=0.5):
+    """q [total, H, D]; one kv tensor [total, D] serving as the shared key and
+    value head (``fwd(q, kv, idx, ...)``); causal top-k index rows and their
+    counts."""
+    q = normal((total, H, D), dtype, seed + 1, amplitude)
+    kv = normal((total, D), dtype, seed + 2, amplitude)
+    idx, length = causal_topk_indices(total, topk, seed + 4)
+    return q, kv, idx, length

@@ -132,3 +132,20 @@ def test_compaction_then_forward(sdpa_lib):
     ref_g, ref_n = oracle.sparse_compact_indices(idx_local, cu, cu, is_causal=True)
     check(out.double().cpu().numpy(), oracle.sdpa_sparse(q, k, v, ref_g, topk_length=ref_n),
           "compact + forward")
+
+
+def test_one_kv_tensor_for_keys_and_values(sdpa_lib):
+    """The same tensor as k and v (one kv tensor, gathered once)."""
+    q, kv, _, idx, length = make(48, 1024, 64, 128, 384, torch.bfloat16, seed=1330)
+    dev = torch.device("cuda")
+    kvd = kv.to(dev)
+    out, lse = sdpa_lib.sdpa_sparse_forward(q.to(dev), kvd, kvd, torch.from_numpy(idx).to(dev),
+                                            torch.from_numpy(length).to(dev), return_lse=True)
+    assert sdpa_lib.sdpa_last_device_status()[0] == 0
+    ref, ref_lse = oracle.sdpa_sparse(q, kv, kv, idx, topk_length=length, return_lse=True)
+    check(out.double().cpu().numpy(), ref, "one kv tensor")
+    # and identical to passing a copy as v
+    out2 = sdpa_lib.sdpa_sparse_forward(q.to(dev), kvd, kvd.clone(),
+                                        torch.from_numpy(idx).to(dev),
+                                        torch.from_numpy(length).to(dev))
+    assert torch.equal(out, out2)
