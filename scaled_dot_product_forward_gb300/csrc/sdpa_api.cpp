@@ -554,6 +554,10 @@ sdpa_status sdpa_sparse_forward(const void* q, const void* k, const void* v, voi
     p.lse_sh = (n_heads > 1) ? lse_stride[1] : 0;
   }
   p.kv_shared = (k == v && (total_k == 1 || k_stride == v_stride)) ? 1 : 0;
+  p.k = k;
+  p.v = v;
+  p.k_row_bytes = 2 * (total_k > 1 ? k_stride : head_dim);
+  p.v_row_bytes = 2 * (total_k > 1 ? v_stride : head_dim);
   p.idx = idx;
   p.idx_st = idx_stride;
   p.topk_length = topk_length;

@@ -49,6 +49,9 @@ struct SparseParams {
   int total_q, total_k, H, topk, n_groups;
   int q_rows;               // rows of the Q box: min(H, 128)
   int kv_shared;            // 1: k and v are one tensor (gather once, use twice)
+  const void* k;            // [total_k, D] rows for the gathers
+  const void* v;
+  int64_t k_row_bytes, v_row_bytes;
   float scale_log2;
   uint64_t wait_limit_ns;
 };

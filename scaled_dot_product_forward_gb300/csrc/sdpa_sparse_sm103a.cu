@@ -40,7 +40,8 @@ namespace {
 
 constexpr int kRows = 128;     // head rows per job (TMEM lanes)
 constexpr int kKeys = 128;     // gathered keys per stage
-constexpr int kThreads = 256;  // WG0: TMA, MMA, 2 idle; WG1: softmax
+constexpr int kThreads = 256;  // WG0: Q loads, MMA, 2 gather warps; WG1: softmax
+constexpr int kGatherWarps = 2;  // warps 2, 3: 64 threads, two key rows each
 constexpr float kRescaleLog2 = 8.0f;
 
 template <int D>
@@ -48,8 +49,9 @@ struct SLayout {
   static constexpr int kChunks = D / 64;
   static constexpr int kChunkBytes = kKeys * 128;  // 128 rows x 64 elements
   static constexpr int kTileBytes = kChunks * kChunkBytes;
+  // K and V stages; with one kv tensor there are no V rows to hold and the
+  // K ring takes both areas (2 * kStages stages).
   static constexpr int kStages = (D == 64) ? 6 : 3;
-  static constexpr int kMaskSlots = kStages + 2;   // see the softmax
   static constexpr int kQ = 0;
   static constexpr int kK = kQ + kTileBytes;
   static constexpr int kV = kK + kStages * kTileBytes;
@@ -63,7 +65,7 @@ static_assert(SLayout<64>::kTotal <= 227 * 1024, "shared memory over the per-CTA
 // TMEM columns: S0 [0,128), S1 [128,256), O [256, 256+D), P [384, 448).
 constexpr uint32_t kColS0 = 0, kColO = 256, kColP = 384, kTmemCols = 512;
 
-constexpr int kMaxStages = 8;
+constexpr int kMaxStages = 12;
 struct SBarriers {
   uint64_t q_full, q_empty;
   uint64_t s_full[2], s_free[2];
@@ -71,8 +73,8 @@ struct SBarriers {
   uint64_t k_full[kMaxStages], k_empty[kMaxStages];
   uint64_t v_full[kMaxStages], v_empty[kMaxStages];
   // Validity of the 128 gathered keys of K tile g, in slot g % kMaskSlots:
-  // word e bit l = key 4l + e (one ballot per lane position); m_full[slot]
-  // completes when the producer has written it.
+  // word w bit i = key 32w + i; m_full[slot] completes when both gather
+  // warps have written their words.
   uint64_t m_full[kMaxStages + 2];
   uint32_t kmask[kMaxStages + 2][4];
   uint32_t tmem_base;
@@ -151,6 +153,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x & 31;
   const uint64_t limit = p.wait_limit_ns;
   const int step = static_cast<int>(gridDim.x);
+  // ring depth (stages of K, and of V when separate) and mask slots (see the
+  // softmax)
+  const int nst = p.kv_shared ? 2 * Lay::kStages : Lay::kStages;
+  const int n_slots = nst + 2;
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
@@ -163,11 +169,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->o_done, 1);
     mbar_init(&bars->o_free, kRows / 32);
     mbar_init(&bars->fin, 1);
-    for (int s = 0; s < Lay::kMaskSlots; ++s) mbar_init(&bars->m_full[s], 1);
-    for (int s = 0; s < Lay::kStages; ++s) {
-      mbar_init(&bars->k_full[s], 1);
+    for (int s = 0; s < kMaxStages + 2; ++s) mbar_init(&bars->m_full[s], kGatherWarps);
+    for (int s = 0; s < kMaxStages; ++s) {
+      mbar_init(&bars->k_full[s], kGatherWarps);
       mbar_init(&bars->k_empty[s], 1);
-      mbar_init(&bars->v_full[s], 1);
+      mbar_init(&bars->v_full[s], kGatherWarps);
       mbar_init(&bars->v_empty[s], 1);
     }
     bars->abort_flag = 0;
@@ -234,16 +240,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // The key mask is read before S's buffer is released: the producer
         // refills this slot only after S of a tile two later has completed,
-        // which needs that release (kMaskSlots = stages + 2), so m_full of
+        // which needs that release (mask slots = stages + 2), so m_full of
         // the slot is at most one phase ahead of this wait.
         uint32_t km[4];
-        if (!warp_swait(&bars->m_full[g % Lay::kMaskSlots], (g / Lay::kMaskSlots) & 1, bars, limit,
+        if (!warp_swait(&bars->m_full[g % n_slots], (g / n_slots) & 1, bars, limit,
                         kSpK)) {
           ok = false;
           break;
         }
         {
-          const volatile uint32_t* src = bars->kmask[g % Lay::kMaskSlots];
+          const volatile uint32_t* src = bars->kmask[g % n_slots];
 #pragma unroll
           for (int e = 0; e < 4; ++e) km[e] = src[e];
         }
@@ -253,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool all_valid = (km[0] & km[1] & km[2] & km[3]) == 0xffffffffu;
         if (!all_valid) {
 #pragma unroll
-          for (int c = 0; c < kKeys; ++c) s[c] = ((km[c & 3] >> (c >> 2)) & 1u) ? s[c] : mval;
+          for (int c = 0; c < kKeys; ++c) s[c] = ((km[c >> 5] >> (c & 31)) & 1u) ? s[c] : mval;
         }
         // row extremum: eight independent chains of three-input max / min
         float e8[8];
@@ -372,12 +378,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tc_fence_before();
   } else if (warp == 0) {
-    // ------------------------------------------------------ loads
+    // ---------------------------------------------------- Q loads
     const bool leader = elect_one();
-    int g = 0, k_end = 0, v_end = 0, jobs = 0;
-    bool ok = true;
+    int jobs = 0;
     SJob job;
-    for (int jj = static_cast<int>(blockIdx.x); ok && job_of(p, jj, job); jj += step) {
+    for (int jj = static_cast<int>(blockIdx.x); job_of(p, jj, job); jj += step) {
       if (job.n_kv == 0) continue;
       if (jobs > 0 && !warp_swait(&bars->q_empty, (jobs - 1) & 1, bars, limit, kSpEmpty)) break;
       if (leader) {
@@ -388,78 +393,100 @@ __global__ void __launch_bounds__(kThreads, 1)
                       job.group * kRows, job.row);
       }
       ++jobs;
+    }
+    if (jobs > 0) swait(&bars->q_full, (jobs - 1) & 1, bars, limit, kSpDrain, false);
+  } else if (warp >= 2) {
+    // ------------------------------------------------- key/value gathers
+    // Thread t (0..63) copies key rows t and t + 64 of every tile, 16 bytes
+    // per cp.async, into the 128-byte-swizzled K-major layout the products
+    // read (piece q of a 128-byte row r lands at q ^ (r & 7)).  A tile is
+    // signalled once its copies are done, `lag` tiles behind the newest, so
+    // later tiles' copies are in flight meanwhile; each thread fences its
+    // completed copies for the tensor core's proxy before the warp arrives.
+    // Warp w (2 or 3) holds key rows 64(w-2) .. +63 of every tile: lane l
+    // loads the indices of rows +l and +32+l; the copies are spread so that
+    // one warp instruction moves whole contiguous rows (D/8 lanes per row).
+    const int wrow = (warp - 2) * 64;
+    const uint8_t* kbase = reinterpret_cast<const uint8_t*>(p.k);
+    const uint8_t* vbase = reinterpret_cast<const uint8_t*>(p.v);
+    constexpr int kPieces = D / 8;          // 16-byte pieces per row
+    constexpr int kRowsPerOp = 32 / kPieces;
+    const int piece = lane % kPieces;
+    const int pc_chunk = piece >> 3, pc_q = piece & 7;
+    int g = 0, signalled = 0;
+    const int lag = min(nst - 2, 4);
+    bool ok = true;
+    auto signal_oldest = [&]() {
+      const int s = signalled % nst;
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&bars->k_full[s]);
+        mbar_arrive(&bars->v_full[s]);
+      }
+      ++signalled;
+    };
+    SJob job;
+    for (int jj = static_cast<int>(blockIdx.x); ok && job_of(p, jj, job); jj += step) {
+      if (job.n_kv == 0) continue;
       const int* irow = p.idx + static_cast<int64_t>(job.row) * p.idx_st;
-      // Lane l gathers keys 4l .. 4l+3 of a tile.  The indices of tile j+1
-      // are loaded while tile j's rows are requested, so the index load's
-      // latency is off the path.
-      int nxt[4];
-      auto load_idx = [&](int j, int (&dst)[4]) {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int t = j * kKeys + 4 * lane + e;
-          dst[e] = (t < job.len) ? __ldg(irow + t) : -1;
-        }
+      auto load_idx = [&](int j, int& a, int& b) {
+        const int ta = j * kKeys + wrow + lane, tb = ta + 32;
+        a = (ta < job.len) ? __ldg(irow + ta) : -1;
+        b = (tb < job.len) ? __ldg(irow + tb) : -1;
       };
-      load_idx(0, nxt);
+      int na, nb;
+      load_idx(0, na, nb);
       for (int j = 0; j < job.n_kv; ++j, ++g) {
-        const int s = g % Lay::kStages;
-        const int use = g / Lay::kStages;
-        // An entry past the row's count or outside [0, total_k) becomes row
-        // 0, removed by the softmax through the mask.
-        int rr[4];
-        uint32_t ballots[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int v = nxt[e];
-          const bool valid = v >= 0 && v < p.total_k;
-          rr[e] = valid ? v : 0;
-          ballots[e] = __ballot_sync(0xffffffffu, valid);
-        }
-        if (j + 1 < job.n_kv) load_idx(j + 1, nxt);
-        if (use > 0 && !warp_swait(&bars->k_empty[s], (use - 1) & 1, bars, limit, kSpEmpty)) {
+        const int s = g % nst;
+        const int use = g / nst;
+        // an entry past the row's count or outside [0, total_k) reads row 0
+        // and is removed by the softmax through the mask
+        const bool va = na >= 0 && na < p.total_k, vb = nb >= 0 && nb < p.total_k;
+        const int ra = va ? na : 0, rb = vb ? nb : 0;
+        const uint32_t ba = __ballot_sync(0xffffffffu, va), bb = __ballot_sync(0xffffffffu, vb);
+        if (j + 1 < job.n_kv) load_idx(j + 1, na, nb);
+        if (use > 0 && (!warp_swait(&bars->k_empty[s], (use - 1) & 1, bars, limit, kSpEmpty) ||
+                        (!p.kv_shared &&
+                         !warp_swait(&bars->v_empty[s], (use - 1) & 1, bars, limit, kSpEmpty)))) {
           ok = false;
           break;
         }
         if (lane == 0) {
-          volatile uint32_t* dst = bars->kmask[g % Lay::kMaskSlots];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) dst[e] = ballots[e];
-          mbar_arrive(&bars->m_full[g % Lay::kMaskSlots]);  // release: the mask is written
+          volatile uint32_t* dst = bars->kmask[g % n_slots];
+          dst[2 * (warp - 2)] = ba;      // keys wrow .. +31
+          dst[2 * (warp - 2) + 1] = bb;  // keys wrow+32 .. +63
+          mbar_arrive(&bars->m_full[g % n_slots]);  // release: the mask is written
         }
-        __syncwarp();
-        if (leader) mbar_arrive_expect_tx(&bars->k_full[s], Lay::kTileBytes);
-        __syncwarp();
-#pragma unroll
-        for (int c = 0; c < Lay::kChunks; ++c)
-          tma_gather4_2d(sK + s * Lay::kTileBytes + c * Lay::kChunkBytes + 4 * lane * 128,
-                         &p.tm_k, &bars->k_full[s], c * 64, rr[0], rr[1], rr[2], rr[3]);
-        k_end = g + 1;
-        if (p.kv_shared) {
-          // one kv tensor: the K rows just gathered are the V rows too
-          if (leader) mbar_arrive(&bars->v_full[s]);
-          __syncwarp();
-          continue;
+        auto copy_rows = [&](const uint8_t* base, int64_t row_bytes, uint8_t* stage) {
+#pragma unroll 4
+          for (int k = 0; k < 64 / kRowsPerOp; ++k) {
+            const int m = k * kRowsPerOp + lane / kPieces;  // row within this warp's 64
+            const int src_reg = (k * kRowsPerOp) >> 5;      // warp-uniform
+            const int ridx = __shfl_sync(0xffffffffu, src_reg ? rb : ra, m & 31);
+            const int r = wrow + m;
+            cp_async_16(stage + pc_chunk * Lay::kChunkBytes + r * 128 + ((pc_q ^ (r & 7)) << 4),
+                        base + static_cast<int64_t>(ridx) * row_bytes + piece * 16);
+          }
+        };
+        copy_rows(kbase, p.k_row_bytes, sK + s * Lay::kTileBytes);
+        if (!p.kv_shared) copy_rows(vbase, p.v_row_bytes, sV + s * Lay::kTileBytes);
+        cp_async_commit();
+        // Keep `lag` tiles of copies in flight (fewer than the ring depth,
+        // so the next tile's stage is always one that was signalled).
+        if (g + 1 - signalled > lag) {
+          switch (lag) {
+            case 1: cp_async_wait<1>(); break;
+            case 2: cp_async_wait<2>(); break;
+            case 3: cp_async_wait<3>(); break;
+            default: cp_async_wait<4>(); break;
+          }
+          while (g + 1 - signalled > lag) signal_oldest();
         }
-        if (use > 0 && !warp_swait(&bars->v_empty[s], (use - 1) & 1, bars, limit, kSpEmpty)) {
-          ok = false;
-          break;
-        }
-        if (leader) mbar_arrive_expect_tx(&bars->v_full[s], Lay::kTileBytes);
-        __syncwarp();
-#pragma unroll
-        for (int c = 0; c < Lay::kChunks; ++c)
-          tma_gather4_2d(sV + s * Lay::kTileBytes + c * Lay::kChunkBytes + 4 * lane * 128,
-                         &p.tm_v, &bars->v_full[s], c * 64, rr[0], rr[1], rr[2], rr[3]);
-        v_end = g + 1;
       }
     }
-    for (int j = max(0, k_end - Lay::kStages); j < k_end; ++j)
-      swait(&bars->k_full[j % Lay::kStages], (j / Lay::kStages) & 1, bars, limit, kSpDrain,
-            false);
-    for (int j = max(0, v_end - Lay::kStages); j < v_end; ++j)
-      swait(&bars->v_full[j % Lay::kStages], (j / Lay::kStages) & 1, bars, limit, kSpDrain,
-            false);
-    if (jobs > 0) swait(&bars->q_full, (jobs - 1) & 1, bars, limit, kSpDrain, false);
+    cp_async_wait<0>();
+    while (signalled < g) signal_oldest();
   } else if (warp == 1) {
     // ------------------------------------------------------ MMA issue
     constexpr uint32_t idS = idesc_f16_f32acc(BF16, false, kRows, kKeys);
@@ -507,24 +534,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int jj = static_cast<int>(blockIdx.x); ok && job_of(p, jj, job); jj += step) {
       if (job.n_kv == 0) continue;
       if (!warp_swait(&bars->q_full, jobs & 1, bars, limit, kSpQ) ||
-          !warp_swait(&bars->k_full[g % Lay::kStages], (g / Lay::kStages) & 1, bars, limit, kSpK) ||
-          !s_next(g % Lay::kStages))
+          !warp_swait(&bars->k_full[g % nst], (g / nst) & 1, bars, limit, kSpK) ||
+          !s_next(g % nst))
         break;
       issued_any = true;
       if (job.n_kv == 1) mma_commit_elect(&bars->q_empty);
       for (int j = 0; j < job.n_kv; ++j) {
         const int gj = g + j;
         if (j + 1 < job.n_kv) {
-          const int s1 = (gj + 1) % Lay::kStages;
-          if (!warp_swait(&bars->k_full[s1], ((gj + 1) / Lay::kStages) & 1, bars, limit, kSpK) ||
+          const int s1 = (gj + 1) % nst;
+          if (!warp_swait(&bars->k_full[s1], ((gj + 1) / nst) & 1, bars, limit, kSpK) ||
               !s_next(s1)) {
             ok = false;
             break;
           }
           if (j + 2 == job.n_kv) mma_commit_elect(&bars->q_empty);
         }
-        const int s = gj % Lay::kStages;
-        if (!warp_swait(&bars->v_full[s], (gj / Lay::kStages) & 1, bars, limit, kSpV) ||
+        const int s = gj % nst;
+        if (!warp_swait(&bars->v_full[s], (gj / nst) & 1, bars, limit, kSpV) ||
             !warp_swait(&bars->p_ready, p_seen & 1, bars, limit, kSpP)) {
           ok = false;
           break;
