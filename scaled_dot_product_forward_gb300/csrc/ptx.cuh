@@ -103,19 +103,6 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, u
       : "memory");
 }
 
-// Row gather: four rows r0..r3 of a 2-D map whose box is one row high,
-// columns [c0, c0 + box width), written to dst as four consecutive box rows
-// (the map's swizzle applies by destination address).
-__device__ __forceinline__ void tma_gather4_2d(void* dst, const CUtensorMap* map, uint64_t* bar,
-                                               int c0, int r0, int r1, int r2, int r3) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_addr(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3),
-      "r"(smem_addr(bar))
-      : "memory");
-}
-
 // 16-byte global -> shared copy through L2 only (cp.async, completion
 // tracked by commit groups).
 __device__ __forceinline__ void cp_async_16(void* smem_dst, const void* gmem_src) {

@@ -537,13 +537,6 @@ sdpa_status sdpa_sparse_forward(const void* q, const void* k, const void* v, voi
     p.q_rows = static_cast<int>(n_heads < 128 ? n_heads : 128);
     const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(p.q_rows), 1};
     if ((s = encode_nd(q, bf16, 3, gdim, gst, box, &p.tm_q)) != SDPA_OK) return s;
-    // K, V: (D, total_k), one-row boxes for the row gathers
-    const cuuint64_t kd[2] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(total_k)};
-    const cuuint64_t ks[1] = {static_cast<cuuint64_t>(total_k > 1 ? k_stride : head_dim) * 2u};
-    const cuuint64_t vs[1] = {static_cast<cuuint64_t>(total_k > 1 ? v_stride : head_dim) * 2u};
-    const cuuint32_t kb[2] = {64, 1};
-    if ((s = encode_nd(k, bf16, 2, kd, ks, kb, &p.tm_k)) != SDPA_OK) return s;
-    if ((s = encode_nd(v, bf16, 2, kd, vs, kb, &p.tm_v)) != SDPA_OK) return s;
   }
   p.out = out;
   p.o_st = so_t;

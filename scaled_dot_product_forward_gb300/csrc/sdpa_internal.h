@@ -36,9 +36,7 @@ struct FwdParams {
 // Sparse top-k attention: query row i (all heads of head group g) attends to
 // the key rows idx[i, 0 .. len_i) of one shared key/value head.
 struct SparseParams {
-  CUtensorMap tm_q;  // 3-D (D, H, total_q), box 64 x 128 x 1 (head group of 128)
-  CUtensorMap tm_k;  // 2-D (D, total_k), box 64 x 1 (row gathers)
-  CUtensorMap tm_v;
+  CUtensorMap tm_q;  // 3-D (D, H, total_q), box 64 x min(H, 128) x 1 (one head group)
   void* out;                // [total_q, H, D]
   int64_t o_st, o_sh;
   float* lse;               // optional [total_q, H]

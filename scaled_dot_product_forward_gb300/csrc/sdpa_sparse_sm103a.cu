@@ -14,10 +14,12 @@
 //   * a job is one query row and a group of up to 128 of its heads: the heads
 //     are the 128 rows of the tensor-core tile (M = 128; groups of fewer heads
 //     are zero-padded by the tensor map), and they share the gathered keys;
-//   * warp 0 loads the job's Q with a 3-D TMA box and gathers K and V rows by
-//     index with TMA row gathers (four rows per instruction, 128 keys per
-//     stage), after checking every index (entries past the row's count or out
-//     of range become row 0 and are removed in the softmax);
+//   * warp 0 loads the job's Q with a 3-D TMA box; warps 2 and 3 gather the
+//     K and V rows by index with coalesced 16-byte cp.async copies (128 keys
+//     per stage, a whole row per instruction group) into the swizzled layout
+//     the tensor core reads, after checking every index (entries past the
+//     row's count or out of range become row 0 and are removed in the
+//     softmax); with one kv tensor the rows are gathered once;
 //   * warp 1 issues S = Q K^T into two alternating TMEM buffers, so S(j+1)
 //     runs while the softmax works on S(j), and O += P V with P in its own
 //     TMEM columns;
@@ -179,11 +181,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bars->abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == 0 && lane == 0) {
-    prefetch_tensormap(&p.tm_q);
-    prefetch_tensormap(&p.tm_k);
-    prefetch_tensormap(&p.tm_v);
-  }
+  if (warp == 0 && lane == 0) prefetch_tensormap(&p.tm_q);
   if (warp == 1) {
     tmem_alloc(&bars->tmem_base, kTmemCols);
     tmem_relinquish();
