@@ -444,11 +444,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int ra = va ? na : 0, rb = vb ? nb : 0;
         const uint32_t ba = __ballot_sync(0xffffffffu, va), bb = __ballot_sync(0xffffffffu, vb);
         if (j + 1 < job.n_kv) load_idx(j + 1, na, nb);
-        if (use > 0 && (!warp_swait(&bars->k_empty[s], (use - 1) & 1, bars, limit, kSpEmpty) ||
-                        (!p.kv_shared &&
-                         !warp_swait(&bars->v_empty[s], (use - 1) & 1, bars, limit, kSpEmpty)))) {
-          ok = false;
-          break;
+        if (use > 0) {
+          const uint32_t par = (use - 1) & 1;
+          const bool free_now = __all_sync(
+              0xffffffffu, mbar_test_wait(&bars->k_empty[s], par) &&
+                               (p.kv_shared || mbar_test_wait(&bars->v_empty[s], par)));
+          if (!free_now) {
+            // About to block on a stage: first finish and signal every tile
+            // still in flight, so the consumers never wait on copies that are
+            // done but not yet announced.
+            cp_async_wait<0>();
+            while (signalled < g) signal_oldest();
+            if (!warp_swait(&bars->k_empty[s], par, bars, limit, kSpEmpty) ||
+                (!p.kv_shared && !warp_swait(&bars->v_empty[s], par, bars, limit, kSpEmpty))) {
+              ok = false;
+              break;
+            }
+          }
         }
         if (lane == 0) {
           volatile uint32_t* dst = bars->kmask[g % n_slots];
