@@ -42,8 +42,16 @@ namespace {
 
 constexpr int kRows = 128;     // head rows per job (TMEM lanes)
 constexpr int kKeys = 128;     // gathered keys per stage
-constexpr int kThreads = 256;  // WG0: Q loads, MMA, 2 gather warps; WG1: softmax
-constexpr int kGatherWarps = 2;  // warps 2, 3: 64 threads, two key rows each
+constexpr int kThreads = 384;  // WG0: Q loads, MMA, 2 idle; WG1: softmax; WG2: gathers
+constexpr int kGatherWarps = 4;  // warps 8..11: one key row per thread
+// Register split: the launch reserves kLaunchRegs per thread (the cap of
+// __launch_bounds__(384, 1)); the softmax warpgroup takes registers from the
+// other two.  128*232 + 256*136 == 384*168.
+constexpr uint32_t kLaunchRegs = 168;
+constexpr uint32_t kRegsSoftmax = 232;
+constexpr uint32_t kRegsOther = 136;
+static_assert(128 * kRegsSoftmax + 256 * kRegsOther <= kThreads * kLaunchRegs,
+              "register split exceeds the launch allocation");
 constexpr float kRescaleLog2 = 8.0f;
 
 template <int D>
@@ -64,14 +72,16 @@ struct SLayout {
 static_assert(SLayout<128>::kTotal <= 227 * 1024, "shared memory over the per-CTA limit");
 static_assert(SLayout<64>::kTotal <= 227 * 1024, "shared memory over the per-CTA limit");
 
-// TMEM columns: S0 [0,128), S1 [128,256), O [256, 256+D), P [384, 448).
+// TMEM columns: S0 [0,128), S1 [128,256), O [256, 256+D), P0 [384,448), P1 [448,512).
 constexpr uint32_t kColS0 = 0, kColO = 256, kColP = 384, kTmemCols = 512;
 
 constexpr int kMaxStages = 12;
 struct SBarriers {
   uint64_t q_full, q_empty;
   uint64_t s_full[2], s_free[2];
-  uint64_t p_ready, o_done, o_free, fin;
+  // P and O += P V double-buffered by tile parity: tile t uses P buffer t & 1,
+  // p_ready[t & 1] and o_done[t & 1] (each completes once per two tiles).
+  uint64_t p_ready[2], o_done[2], o_free, fin;
   uint64_t k_full[kMaxStages], k_empty[kMaxStages];
   uint64_t v_full[kMaxStages], v_empty[kMaxStages];
   // Validity of the 128 gathered keys of K tile g, in slot g % kMaskSlots:
@@ -167,8 +177,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->s_full[b], 1);
       mbar_init(&bars->s_free[b], kRows / 32);
     }
-    mbar_init(&bars->p_ready, kRows / 32);
-    mbar_init(&bars->o_done, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bars->p_ready[b], kRows / 32);
+      mbar_init(&bars->o_done[b], 1);
+    }
     mbar_init(&bars->o_free, kRows / 32);
     mbar_init(&bars->fin, 1);
     for (int s = 0; s < kMaxStages + 2; ++s) mbar_init(&bars->m_full[s], kGatherWarps);
@@ -193,15 +205,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   grid_launch_dependents();
   const uint32_t tmem = bars->tmem_base;
 
-  if (warp >= 4) {
+  if (warp >= 4 && warp < 8) {
     // ---------------------------------------------------- softmax warps
+    regs_increase<kRegsSoftmax>();
     const int wq = warp & 3;
     const int r = wq * 32 + lane;  // head row within the group
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
     const float sl2 = p.scale_log2;
     const bool pos_scale = sl2 >= 0.0f;
     const float mval = pos_scale ? -INFINITY : INFINITY;
-    uint32_t ns = 0, o_seen = 0;
+    uint32_t ns = 0;
     int g = 0;  // K tile counter (mask slot)
     bool ok = true;
     SJob job;
@@ -311,16 +324,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         add2_acc(rs[4], rs[5], rs[6], rs[7]);
         add2_acc(rs[0], rs[1], rs[4], rs[5]);
         l += rs[0] + rs[1];
-        if (j > 0) {
-          // PV(j-1) must be complete before O is rescaled or P is replaced.
-          // Waited here, in order, before the p_ready arrival below.
-          if (!warp_swait(&bars->o_done, o_seen & 1, bars, limit, kSpO)) {
+        // Global tile index t (all jobs of this CTA).  Each wait below is
+        // on a barrier whose next phase needs this tile's P, so it can never
+        // fall two phases behind.
+        const uint32_t t = ns - 1;
+        if (j > 0 && __any_sync(0xffffffffu, need)) {
+          // O is rescaled once PV(t-1) (and so every earlier product) is done
+          if (!warp_swait(&bars->o_done[(t - 1) & 1], ((t - 1) >> 1) & 1, bars, limit, kSpO)) {
             ok = false;
             break;
           }
-          ++o_seen;
           tc_fence_after();
-          if (__any_sync(0xffffffffu, need)) {
+          {
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
               uint32_t o[32];
@@ -333,18 +348,28 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        tmem_st32(tmem + kColP + lane_off, pk);
-        tmem_st32(tmem + kColP + lane_off + 32, pk + 32);
+        // P buffer t & 1 is free once PV(t-2) is done.
+        const uint32_t pb = t & 1;
+        if (t >= 2) {
+          if (!warp_swait(&bars->o_done[pb], ((t >> 1) - 1) & 1, bars, limit, kSpO)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+        }
+        tmem_st32(tmem + kColP + pb * 64 + lane_off, pk);
+        tmem_st32(tmem + kColP + pb * 64 + lane_off + 32, pk + 32);
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->p_ready);
+        if (lane == 0) mbar_arrive(&bars->p_ready[pb]);
       }
-      if (!ok || !warp_swait(&bars->o_done, o_seen & 1, bars, limit, kSpO)) {
+      // the job's last product (and so all of them) must be done
+      const uint32_t t_last = ns - 1;
+      if (!ok || !warp_swait(&bars->o_done[t_last & 1], (t_last >> 1) & 1, bars, limit, kSpO)) {
         ok = false;
         break;
       }
-      ++o_seen;
       tc_fence_after();
       const float inv_l = (l > 0.0f) ? (1.0f / l) : 0.0f;
       if (h < p.H && p.lse != nullptr) {
@@ -375,7 +400,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(&bars->o_free);
     }
     tc_fence_before();
-  } else if (warp == 0) {
+  } else {
+  regs_decrease<kRegsOther>();
+  if (warp == 0) {
     // ---------------------------------------------------- Q loads
     const bool leader = elect_one();
     int jobs = 0;
@@ -393,18 +420,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++jobs;
     }
     if (jobs > 0) swait(&bars->q_full, (jobs - 1) & 1, bars, limit, kSpDrain, false);
-  } else if (warp >= 2) {
+  } else if (warp >= 8) {
     // ------------------------------------------------- key/value gathers
-    // Thread t (0..63) copies key rows t and t + 64 of every tile, 16 bytes
+    // Warp w (8..11) copies key rows 32(w-8) .. +31 of every tile, 16 bytes
     // per cp.async, into the 128-byte-swizzled K-major layout the products
-    // read (piece q of a 128-byte row r lands at q ^ (r & 7)).  A tile is
-    // signalled once its copies are done, `lag` tiles behind the newest, so
-    // later tiles' copies are in flight meanwhile; each thread fences its
+    // read (piece q of a 128-byte row r lands at q ^ (r & 7)); lane l loads
+    // the index of row +l, and the copies are spread so that one warp
+    // instruction moves whole contiguous rows (D/8 lanes per row).  A tile
+    // is signalled once its copies are done, `lag` tiles behind the newest,
+    // so later tiles' copies are in flight meanwhile; each thread fences its
     // completed copies for the tensor core's proxy before the warp arrives.
-    // Warp w (2 or 3) holds key rows 64(w-2) .. +63 of every tile: lane l
-    // loads the indices of rows +l and +32+l; the copies are spread so that
-    // one warp instruction moves whole contiguous rows (D/8 lanes per row).
-    const int wrow = (warp - 2) * 64;
+    const int wrow = (warp - 8) * 32;
     const uint8_t* kbase = reinterpret_cast<const uint8_t*>(p.k);
     const uint8_t* vbase = reinterpret_cast<const uint8_t*>(p.v);
     constexpr int kPieces = D / 8;          // 16-byte pieces per row
@@ -428,22 +454,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int jj = static_cast<int>(blockIdx.x); ok && job_of(p, jj, job); jj += step) {
       if (job.n_kv == 0) continue;
       const int* irow = p.idx + static_cast<int64_t>(job.row) * p.idx_st;
-      auto load_idx = [&](int j, int& a, int& b) {
-        const int ta = j * kKeys + wrow + lane, tb = ta + 32;
-        a = (ta < job.len) ? __ldg(irow + ta) : -1;
-        b = (tb < job.len) ? __ldg(irow + tb) : -1;
+      auto load_idx = [&](int j) {
+        const int ta = j * kKeys + wrow + lane;
+        return (ta < job.len) ? __ldg(irow + ta) : -1;
       };
-      int na, nb;
-      load_idx(0, na, nb);
+      int na = load_idx(0);
       for (int j = 0; j < job.n_kv; ++j, ++g) {
         const int s = g % nst;
         const int use = g / nst;
         // an entry past the row's count or outside [0, total_k) reads row 0
         // and is removed by the softmax through the mask
-        const bool va = na >= 0 && na < p.total_k, vb = nb >= 0 && nb < p.total_k;
-        const int ra = va ? na : 0, rb = vb ? nb : 0;
-        const uint32_t ba = __ballot_sync(0xffffffffu, va), bb = __ballot_sync(0xffffffffu, vb);
-        if (j + 1 < job.n_kv) load_idx(j + 1, na, nb);
+        const bool va = na >= 0 && na < p.total_k;
+        const int ra = va ? na : 0;
+        const uint32_t ba = __ballot_sync(0xffffffffu, va);
+        if (j + 1 < job.n_kv) na = load_idx(j + 1);
         if (use > 0) {
           const uint32_t par = (use - 1) & 1;
           const bool free_now = __all_sync(
@@ -464,16 +488,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (lane == 0) {
           volatile uint32_t* dst = bars->kmask[g % n_slots];
-          dst[2 * (warp - 2)] = ba;      // keys wrow .. +31
-          dst[2 * (warp - 2) + 1] = bb;  // keys wrow+32 .. +63
+          dst[warp - 8] = ba;  // keys wrow .. +31
           mbar_arrive(&bars->m_full[g % n_slots]);  // release: the mask is written
         }
         auto copy_rows = [&](const uint8_t* base, int64_t row_bytes, uint8_t* stage) {
 #pragma unroll 4
-          for (int k = 0; k < 64 / kRowsPerOp; ++k) {
-            const int m = k * kRowsPerOp + lane / kPieces;  // row within this warp's 64
-            const int src_reg = (k * kRowsPerOp) >> 5;      // warp-uniform
-            const int ridx = __shfl_sync(0xffffffffu, src_reg ? rb : ra, m & 31);
+          for (int k = 0; k < 32 / kRowsPerOp; ++k) {
+            const int m = k * kRowsPerOp + lane / kPieces;  // row within this warp's 32
+            const int ridx = __shfl_sync(0xffffffffu, ra, m);
             const int r = wrow + m;
             cp_async_16(stage + pc_chunk * Lay::kChunkBytes + r * 128 + ((pc_q ^ (r & 7)) << 4),
                         base + static_cast<int64_t>(ridx) * row_bytes + piece * 16);
@@ -517,16 +539,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       mma_commit_elect(&bars->s_full[buf]);
     };
-    auto issue_pv = [&](int s, bool accumulate) {
+    auto issue_pv = [&](int s, uint32_t pb, bool accumulate) {
       const uint32_t b0 = v_lo + static_cast<uint32_t>(s * (Lay::kTileBytes >> 4));
 #pragma unroll
       for (int kk = 0; kk < kKeys / 16; ++kk)
-        mma_ts_elect<kHi>(tmem + kColO, tmem + kColP + kk * 8, b0 + ((kk * 16 * 128) >> 4), idPV,
-                          (accumulate || kk > 0) ? 1u : 0u);
-      mma_commit_elect(&bars->o_done);
+        mma_ts_elect<kHi>(tmem + kColO, tmem + kColP + pb * 64 + kk * 8,
+                          b0 + ((kk * 16 * 128) >> 4), idPV, (accumulate || kk > 0) ? 1u : 0u);
+      mma_commit_elect(&bars->o_done[pb]);
     };
     int g = 0, jobs = 0;
-    uint32_t ns = 0, p_seen = 0;
+    uint32_t ns = 0;
     bool ok = true;
     SJob job;
     // S into the buffer of S(ns); its previous contents (S(ns-2)) must be in
@@ -562,11 +584,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const int s = gj % nst;
         if (!warp_swait(&bars->v_full[s], (gj / nst) & 1, bars, limit, kSpV) ||
-            !warp_swait(&bars->p_ready, p_seen & 1, bars, limit, kSpP)) {
+            !warp_swait(&bars->p_ready[gj & 1], (gj >> 1) & 1, bars, limit, kSpP)) {
           ok = false;
           break;
         }
-        ++p_seen;
         // The job's first product overwrites O: the previous epilogue must
         // have read it.
         if (j == 0 && jobs > 0 &&
@@ -575,7 +596,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
-        issue_pv(s, j > 0);
+        issue_pv(s, static_cast<uint32_t>(gj) & 1, j > 0);
         mma_commit_elect(p.kv_shared ? &bars->k_empty[s] : &bars->v_empty[s]);
       }
       g += job.n_kv;
@@ -586,6 +607,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       swait(&bars->fin, 0, bars, limit, kSpDrain, false);
     }
   }
+  }  // warpgroups 0 and 2
 
   __syncthreads();
   if (warp == 1) {
@@ -634,7 +656,13 @@ cudaError_t launch_sparse_one(const sdpa_impl::SparseParams& p, int max_ctas,
   constexpr int smem = SLayout<D>::kTotal;
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    // The register split assumes kLaunchRegs per thread at launch; never
+    // launch a build where that does not hold (setmaxnreg would wait).
+    cudaFuncAttributes fa{};
+    cudaError_t e = cudaFuncGetAttributes(&fa, kern);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs != static_cast<int>(kLaunchRegs)) return cudaErrorInvalidConfiguration;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     configured = true;
   }
