@@ -71,7 +71,7 @@ def test_small_full(sdpa_lib, B, H, L, D, dtype, causal):
     check(out.double().cpu().numpy(), ref, f"{B}x{H}x{L}x{D}")
 
 
-@pytest.mark.parametrize("L,D", [(256, 64), (250, 64), (300, 128), (130, 64)])
+@pytest.mark.parametrize("L,D", [(256, 64), (250, 64), (300, 128), (130, 64), (400, 64), (272, 128)])
 def test_masked_small(sdpa_lib, L, D):
     q, k, v = sdpa_inputs.custom((1, 2, L, D), dtype=torch.float16, seed=7 + L)
     mask = sdpa_inputs.bernoulli_mask(L, 0.3, seed=50 + L, n_full_rows=5, rows_seed=51 + L)
