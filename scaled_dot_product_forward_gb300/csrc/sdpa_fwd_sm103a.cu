@@ -384,7 +384,13 @@ __device__ __forceinline__ void for_each_job(const sdpa_impl::FwdParams& p, F&& 
     const int lane = static_cast<int>(threadIdx.x & 31);
     SeqCursor c{0, 0, 0, min(max(__ldg(p.cu_seqlens), 0), p.L), 0, 0, 0, 0};
     cursor_load(p, c, lane);
-    for (int u = static_cast<int>(blockIdx.x);; u += step) {
+    // Units in snake order over the CTAs (0..G-1, then G-1..0, ...): units
+    // of different documents cost differently, and alternating the
+    // direction evens out what each CTA collects.  The sequence still grows,
+    // as the cursor needs.
+    const int cta = static_cast<int>(blockIdx.x);
+    for (int r = 0;; ++r) {
+      const int u = r * step + ((r & 1) ? step - 1 - cta : cta);
       Work w;
       int k, n_tiles;
       if (!cursor_find<MODE>(p, c, lane, u, k, n_tiles, w)) return;
