@@ -42,11 +42,13 @@ UNIT = "TFLOP/s"
 FALLBACK_BF16_TFLOPS = 1900.0
 KERNEL_SOURCES = ["scaled_dot_product_forward_gb300/csrc/sdpa_fwd_sm103a.cu",
                   "scaled_dot_product_forward_gb300/csrc/ptx.cuh"]
+SPARSE_SOURCES = ["scaled_dot_product_forward_gb300/csrc/sdpa_sparse_sm103a.cu",
+                  "scaled_dot_product_forward_gb300/csrc/ptx.cuh"]
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(sources=None) -> str:
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in sources or KERNEL_SOURCES:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -62,9 +64,10 @@ def load_peaks():
         return FALLBACK_BF16_TFLOPS, 6800.0, "fallback"
 
 
-def load_traffic(workload_id: int):
+def load_traffic(workload_id, sources=None):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel source (else None)."""
+    on the current kernel source (else None).  ``workload_id`` is a dense
+    workload number or "sparse"."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
@@ -72,7 +75,7 @@ def load_traffic(workload_id: int):
     except (OSError, ValueError):
         return None
     entry = t.get(str(workload_id))
-    if not entry or entry.get("kernel_source_hash") != kernel_source_hash():
+    if not entry or entry.get("kernel_source_hash") != kernel_source_hash(sources):
         return None
     return entry.get("dram_bytes_per_launch")
 
@@ -437,7 +440,8 @@ def extra_leg(args, path):
             "config": config,
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
                          "frac": achieved / peak, "peak_source": f"{peak_kind} dense bf16 (burst)",
-                         "traffic": None, "alg_flops_per_launch": flops, "mean_launch_ms": ms},
+                         "traffic": load_traffic("sparse", SPARSE_SOURCES) if path == "sparse" else None,
+                         "alg_flops_per_launch": flops, "mean_launch_ms": ms},
             "e2e": {"value": flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
                     "h2d_bytes_per_step": sum(x.numel() * x.element_size() for x in ins),
                     "d2h_bytes_per_step": out.numel() * out.element_size(),
