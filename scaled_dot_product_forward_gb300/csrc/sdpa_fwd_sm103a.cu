@@ -449,23 +449,62 @@ __device__ __forceinline__ bool softmax_job(const sdpa_impl::FwdParams& p, const
     if constexpr (MODE == sdpa_impl::kMaskExplicit) {
       const bool row_ok = row_g < w.len;
       const uint8_t* mrow = p.mask + static_cast<int64_t>(row_ok ? row_g : 0) * p.L + col0;
-      if (p.mask_vec16 && !tail && row_ok) {
-        uint4 x[kBlockN / 16];
+      if (p.mask_vec16 && !tail && row_g - lane + 31 < w.len) {
+        static_assert(kBlockN == 128, "the mask transpose assumes 128-key tiles");
+        // Coalesced: lane (g, c) = (lane / 8, lane % 8) reads 16 bytes of
+        // row 8g + i at keys 16c.. for i = 0..7, so each load instruction
+        // covers four whole 128-byte row segments, and turns them into 16
+        // bits.  An 8 x 8 transpose of 16-bit values inside each group of
+        // eight lanes (three butterfly stages) then gives every lane the 128
+        // bits of its own row: word k = keys 32k..32k+31.
+        const int g8 = lane >> 3, c8 = lane & 7;
+        const uint8_t* mbase =
+            p.mask + static_cast<int64_t>(row_g - lane + 8 * g8) * p.L + col0 + 16 * c8;
+        uint4 x[8];
 #pragma unroll
-        for (int v = 0; v < kBlockN / 16; ++v) x[v] = __ldg(reinterpret_cast<const uint4*>(mrow) + v);
+        for (int i = 0; i < 8; ++i)
+          x[i] = __ldg(reinterpret_cast<const uint4*>(mbase + static_cast<int64_t>(i) * p.L));
+        uint32_t wv[4];
 #pragma unroll
-        for (int w32 = 0; w32 < kBlockN / 32; ++w32) {
-          uint32_t bits = 0;
-#pragma unroll
-          for (int q4 = 0; q4 < 8; ++q4) {  // four bytes at a time
-            const int b0 = 32 * w32 + 4 * q4;
-            const uint4 xv = x[b0 >> 4];
-            const int wi = (b0 & 15) >> 2;
-            const uint32_t word = (wi == 0) ? xv.x : (wi == 1) ? xv.y : (wi == 2) ? xv.z : xv.w;
-            bits |= nonzero_byte_bits(word) << (4 * q4);
-          }
-          mbits[w32] = bits;
+        for (int k2 = 0; k2 < 4; ++k2) {
+          const uint4 a = x[2 * k2], b = x[2 * k2 + 1];
+          const uint32_t ha = nonzero_byte_bits(a.x) | (nonzero_byte_bits(a.y) << 4) |
+                              (nonzero_byte_bits(a.z) << 8) | (nonzero_byte_bits(a.w) << 12);
+          const uint32_t hb = nonzero_byte_bits(b.x) | (nonzero_byte_bits(b.y) << 4) |
+                              (nonzero_byte_bits(b.z) << 8) | (nonzero_byte_bits(b.w) << 12);
+          wv[k2] = ha | (hb << 16);  // rows 8g+2k2 (low) and 8g+2k2+1 (high), keys 16c..
         }
+        {  // swap the off-diagonal 4 x 4 blocks (lane bit 2 <-> element bit 2)
+          const bool hi = (c8 & 4) != 0;
+          const uint32_t r0 = __shfl_xor_sync(0xffffffffu, hi ? wv[0] : wv[2], 4);
+          const uint32_t r1 = __shfl_xor_sync(0xffffffffu, hi ? wv[1] : wv[3], 4);
+          if (hi) { wv[0] = r0; wv[1] = r1; } else { wv[2] = r0; wv[3] = r1; }
+        }
+        {  // 2 x 2 blocks inside each (lane bit 1 <-> element bit 1)
+          const bool hi = (c8 & 2) != 0;
+          const uint32_t r0 = __shfl_xor_sync(0xffffffffu, hi ? wv[0] : wv[1], 2);
+          const uint32_t r1 = __shfl_xor_sync(0xffffffffu, hi ? wv[2] : wv[3], 2);
+          if (hi) { wv[0] = r0; wv[2] = r1; } else { wv[1] = r0; wv[3] = r1; }
+        }
+        {  // single elements (lane bit 0 <-> the 16-bit half of a word)
+          const bool hi = (c8 & 1) != 0;
+          const uint32_t sel = hi ? 0x5410u : 0x7632u;
+          const uint32_t r0 = __shfl_xor_sync(0xffffffffu, __byte_perm(wv[0], wv[1], sel), 1);
+          const uint32_t r1 = __shfl_xor_sync(0xffffffffu, __byte_perm(wv[2], wv[3], sel), 1);
+          if (hi) {
+            wv[0] = __byte_perm(r0, wv[0], 0x7610u);
+            wv[1] = __byte_perm(r0, wv[1], 0x7632u);
+            wv[2] = __byte_perm(r1, wv[2], 0x7610u);
+            wv[3] = __byte_perm(r1, wv[3], 0x7632u);
+          } else {
+            wv[0] = __byte_perm(wv[0], r0, 0x5410u);
+            wv[1] = __byte_perm(wv[1], r0, 0x7610u);
+            wv[2] = __byte_perm(wv[2], r1, 0x5410u);
+            wv[3] = __byte_perm(wv[3], r1, 0x7610u);
+          }
+        }
+#pragma unroll
+        for (int k2 = 0; k2 < 4; ++k2) mbits[k2] = wv[k2];
       } else {
 #pragma unroll
         for (int w32 = 0; w32 < kBlockN / 32; ++w32) {
