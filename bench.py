@@ -314,9 +314,10 @@ def gpu_leg(args, w, rank, world):
         with torch.cuda.stream(stream):  # replay() launches on the current stream
             graph.replay()
     else:
+        timed = plan_step if args.plan else step
         for i in range(args.steps):
             starts[i].record(stream)
-            step()
+            timed()
             ends[i].record(stream)
     t_end.record(stream)
     torch.cuda.synchronize(dev)
@@ -489,6 +490,9 @@ def main(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--plan", action="store_true",
+                    help="time sdpa_plan_launch per step (with a mask: the mask summary kernel "
+                         "and the forward, both inside each timed launch)")
     ap.add_argument("--graph", action="store_true",
                     help="time a CUDA graph of K plan launches (no host gaps between kernels)")
     ap.add_argument("--path", choices=["dense", "varlen", "sparse"], default="dense",
@@ -507,7 +511,10 @@ def main(argv=None):
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     config = {"workload": w.name, "B": w.B, "H": w.H, "L": w.L, "D": w.D,
-              "launch": "cuda graph of plan launches" if args.graph else "sdpa_forward per step",
+              "launch": ("cuda graph of plan launches" if args.graph else
+                         "sdpa_plan_launch per step" if args.plan else "sdpa_forward per step") +
+                        (" (mask summary kernel + forward)" if (args.graph or args.plan) and
+                         w.p_masked is not None else ""),
               "is_causal": w.is_causal, "mask": w.p_masked is not None,
               "rank": w.rank, "scale": "1/sqrt(D)",
               "l2": "no flush: q, k, v, out total %.0f MB > 129 MB L2" % (
@@ -567,7 +574,8 @@ def main(argv=None):
             "e2e": {"value": world * r["flops"] / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
                     "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"],
                     "ms_per_step": e2e_ms},
-            "gpu_launches": args.steps,
+            "gpu_launches": args.steps * (2 if (args.graph or args.plan) and
+                                          w.p_masked is not None else 1),
             "host_us_per_call": r["host_us"],
             "clocks": r["clocks"]}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -131,6 +131,16 @@ SDPA_API sdpa_status sdpa_forward(const void* q, const void* k, const void* v, v
  *                         SDPA_ERR_ARG if the current device is not the
  *                         plan's.  Safe to call from several threads on
  *                         different streams, and inside CUDA graph capture.
+ *                         A plan with a mask first launches the mask summary
+ *                         (see sdpa_mask_tiles) into device memory the plan
+ *                         allocated at creation (n^2 * 2049 bytes for n =
+ *                         ceil(L / 128); SDPA_ERR_CUDA from sdpa_plan_create
+ *                         when that allocation fails), then the forward,
+ *                         which skips the key tiles that remove every key
+ *                         for both query tiles of its job and reads 16 bytes
+ *                         of mask per row and tile.  Concurrent launches of
+ *                         one plan write identical summary bytes as long as
+ *                         the mask's contents do not change meanwhile.
  * sdpa_plan_destroy     : frees the plan (NULL is ignored).  Work already
  *                         enqueued is unaffected.
  */
@@ -146,6 +156,28 @@ SDPA_API sdpa_status sdpa_plan_set_pointers(sdpa_plan* plan, const void* q, cons
                                             const void* v, void* out, const uint8_t* mask);
 SDPA_API sdpa_status sdpa_plan_launch(const sdpa_plan* plan, void* stream);
 SDPA_API void sdpa_plan_destroy(sdpa_plan* plan);
+
+/*
+ * sdpa_mask_tiles -- the tile summary of an explicit mask (the mask-tile
+ * skip bitmap masked plans use), written into caller-owned memory.
+ *
+ * The [L, L] mask (DEVICE, row-major bytes, nonzero = removed: the
+ * masked_fill polarity of "Profiling attention in PyTorch: kernels, backends
+ * and where the time goes", news.bpdata.com, section "Naiv causal attention") is cut
+ * into n x n tiles of 128 x 128, n = ceil(L / 128).  For tile (qt, kt):
+ *   tile_bits  : DEVICE, 16-byte aligned, n*n*128*16 bytes.  Row r of the
+ *                tile is four 32-bit words at byte ((qt*n + kt)*128 + r)*16;
+ *                bit c of word w is 1 when key kt*128 + 32w + c is removed
+ *                for query qt*128 + r.  Keys and rows past L read as removed.
+ *   tile_class : DEVICE, n*n bytes at qt*n + kt: 0 = no entry inside [L, L]
+ *                is removed, 1 = some are, 2 = all are.
+ * Asynchronous on `stream` (PDL launch: it waits for the previous kernel in
+ * the stream before reading the mask).  Errors: SDPA_ERR_NULL,
+ * SDPA_ERR_SHAPE (L < 1 or n > 65535), SDPA_ERR_LAYOUT (tile_bits not 16-byte
+ * aligned), SDPA_ERR_CUDA.
+ */
+SDPA_API sdpa_status sdpa_mask_tiles(const uint8_t* mask, int64_t L, void* tile_bits,
+                                     uint8_t* tile_class, void* stream);
 
 /*
  * sdpa_forward_lse -- sdpa_forward that also writes, per query row, the

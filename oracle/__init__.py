@@ -243,6 +243,40 @@ def sparse_compact_indices(idx_local, cu_seqlens_q, cu_seqlens_k, is_causal=True
     return out, length
 
 
+def mask_tiles(mask, tile=128):
+    """Tile summary of an explicit [L, L] mask (nonzero = removed, the
+    masked_fill polarity of the naive module in "Profiling attention in
+    PyTorch: kernels, backends and where the time goes", news.bpdata.com):
+    the mask-tile skip bitmap of the per-shape tuning row.  For each tile
+    (qt, kt) of tile x tile entries: ``bits[qt, kt, r, w]`` (uint32) has bit c
+    set when key kt*tile + 32w + c is removed for query qt*tile + r, with
+    keys and rows outside [0, L) counted as removed; ``classes[qt, kt]`` is 0
+    when no entry inside [L, L] is removed, 2 when all are, else 1.  Plain
+    loops over the definition; returns (bits, classes)."""
+    m = np.asarray(mask)
+    L = m.shape[0]
+    assert m.shape == (L, L) and tile % 32 == 0
+    n = (L + tile - 1) // tile
+    bits = np.zeros((n, n, tile, tile // 32), dtype=np.uint32)
+    classes = np.zeros((n, n), dtype=np.uint8)
+    for qt in range(n):
+        for kt in range(n):
+            seen_removed = seen_kept = False
+            for r in range(tile):
+                i = qt * tile + r
+                for c in range(tile):
+                    j = kt * tile + c
+                    inside = i < L and j < L
+                    removed = (not inside) or m[i, j] != 0
+                    if removed:
+                        bits[qt, kt, r, c // 32] |= np.uint32(1 << (c % 32))
+                    if inside:
+                        seen_removed = seen_removed or removed
+                        seen_kept = seen_kept or not removed
+            classes[qt, kt] = 0 if not seen_removed else (2 if not seen_kept else 1)
+    return bits, classes
+
+
 def sdpa_sparse(q, k, v, idx, topk_length=None, scale=None, return_lse=False):
     """Sparse top-k attention, fp64: query row ``i`` (all of its heads)
     attends to the key rows ``idx[i, :topk_length[i]]`` of one shared key /

@@ -20,7 +20,8 @@ from . import _build
 __all__ = ["sdpa_forward", "sdpa_forward_raw", "sdpa_status_string", "sdpa_last_device_status",
            "sdpa_version", "SdpaError", "load_library", "LIB_PATH", "STATUS",
            "sdpa_debug_set_wait_limit_ns", "sdpa_debug_withhold_q_load", "sdpa_debug_exp2_poly",
-           "sdpa_forward_varlen", "sdpa_sparse_forward", "sdpa_sparse_compact", "SdpaPlan"]
+           "sdpa_forward_varlen", "sdpa_sparse_forward", "sdpa_sparse_compact", "SdpaPlan",
+           "sdpa_mask_tiles"]
 
 LIB_PATH = _build.LIB_PATH
 
@@ -98,6 +99,8 @@ def load_library(path: str | None = None):
                                         ctypes.c_int64, ctypes.c_int64, vp, vp, ctypes.c_int64,
                                         ctypes.c_int, vp]
     lib.sdpa_sparse_compact.restype = ctypes.c_int
+    lib.sdpa_mask_tiles.argtypes = [vp, ctypes.c_int64, vp, vp, vp]
+    lib.sdpa_mask_tiles.restype = ctypes.c_int
     if path is None:
         _lib = lib
     return lib
@@ -333,6 +336,31 @@ def sdpa_sparse_compact(idx_local, cu_seqlens_q, cu_seqlens_k, *, is_causal: boo
     if rc != 0:
         raise SdpaError(rc, "sdpa_sparse_compact")
     return idx_global, length
+
+
+def sdpa_mask_tiles(mask, *, stream=None):
+    """Mask summary (sdpa_mask_tiles) of a device [L, L] bool/uint8 mask
+    (nonzero = removed): (bits int32 [n, n, 128, 4], classes uint8 [n, n])
+    for n = ceil(L / 128) tiles of 128 x 128; bits[qt, kt, r, w] bit c = key
+    kt*128 + 32w + c removed for row qt*128 + r (past L: removed); class 0 =
+    the tile removes no entry inside [L, L], 1 = some, 2 = all."""
+    import torch
+
+    if mask.dim() != 2 or mask.shape[0] != mask.shape[1] or not mask.is_contiguous():
+        raise SdpaError(3)
+    if mask.dtype not in (torch.bool, torch.uint8):
+        raise SdpaError(4)
+    L = mask.shape[0]
+    n = (L + 127) // 128
+    bits = torch.empty((n, n, 128, 4), dtype=torch.int32, device=mask.device)
+    classes = torch.empty((n, n), dtype=torch.uint8, device=mask.device)
+    st = (stream if stream is not None else torch.cuda.current_stream(mask.device)).cuda_stream
+    rc = load_library().sdpa_mask_tiles(
+        ctypes.c_void_p(mask.data_ptr()), L, ctypes.c_void_p(bits.data_ptr()),
+        ctypes.c_void_p(classes.data_ptr()), ctypes.c_void_p(st) if st else None)
+    if rc != 0:
+        raise SdpaError(rc, "sdpa_mask_tiles")
+    return bits, classes
 
 
 def _dtype_code(q):

@@ -303,9 +303,29 @@ sdpa_status launch_prepared(const Prepared& pr, void* stream) {
   sdpa_impl::FwdParams p = pr.p;
   p.debug_withhold_q = g_withhold_q.load(std::memory_order_relaxed);
   p.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
+  if (p.tile_class != nullptr) {
+    // The mask summary is rebuilt from the mask on every launch (the mask's
+    // contents may change between launches); the forward waits for it.
+    sdpa_impl::MaskTilesParams mt{};
+    mt.mask = p.mask;
+    mt.L = p.L;
+    mt.n_tiles = p.n_tiles;
+    mt.vec16 = p.mask_vec16;
+    mt.bits = reinterpret_cast<uint16_t*>(const_cast<uint4*>(p.tile_bits));
+    mt.tile_class = const_cast<uint8_t*>(p.tile_class);
+    if (sdpa_impl::launch_mask_tiles(mt, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+      return SDPA_ERR_CUDA;
+  }
   const cudaError_t e = sdpa_impl::launch_forward(p, pr.head_dim, pr.mode, pr.bf16, pr.sms,
                                                   static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;
+}
+
+// Bytes of a mask summary for an [L, L] mask: 2 KB of row bits and one class
+// byte per 128 x 128 tile.
+uint64_t mask_tiles_bytes(int64_t L) {
+  const uint64_t n = static_cast<uint64_t>((L + 127) / 128);
+  return n * n * (128u * 16u + 1u);
 }
 
 using ReplaceAddressFn = CUresult (*)(CUtensorMap*, void*);
@@ -360,6 +380,16 @@ struct sdpa_plan {
   int is_causal;
   float scale;
   sdpa_dtype dtype;
+  void* mask_tiles = nullptr;  // device: the mask summary (masked plans only)
+
+  ~sdpa_plan() {
+    if (mask_tiles == nullptr) return;
+    int cur = -1;
+    const bool restore = cudaGetDevice(&cur) == cudaSuccess && cur != pr.device;
+    if (restore) cudaSetDevice(pr.device);
+    cudaFree(mask_tiles);
+    if (restore) cudaSetDevice(cur);
+  }
 };
 
 extern "C" {
@@ -638,6 +668,26 @@ sdpa_status sdpa_plan_create(sdpa_plan** plan, const void* q, const void* k, con
   pl->is_causal = is_causal;
   pl->scale = scale;
   pl->dtype = dtype;
+  if (mask != nullptr && pl->pr.p.n_tiles > 65535) {
+    delete pl;
+    return SDPA_ERR_SHAPE;
+  }
+  if (mask != nullptr) {
+    // A masked plan owns a summary of its mask (per 128 x 128 tile: the rows
+    // as bits and whether the tile removes no, some or every key), rebuilt on
+    // each launch; the forward then reads 16 bytes per row and tile instead of
+    // 128, skips the select in tiles that remove nothing and skips tiles that
+    // remove everything for both query tiles of a job.
+    const uint64_t bytes = mask_tiles_bytes(pl->pr.p.L);
+    const uint64_t n2 = bytes / (128u * 16u + 1u);
+    if (cudaMalloc(&pl->mask_tiles, bytes) != cudaSuccess) {
+      pl->mask_tiles = nullptr;
+      delete pl;
+      return SDPA_ERR_CUDA;
+    }
+    pl->pr.p.tile_bits = static_cast<const uint4*>(pl->mask_tiles);
+    pl->pr.p.tile_class = static_cast<const uint8_t*>(pl->mask_tiles) + n2 * 128u * 16u;
+  }
   const int64_t* st[4] = {q_stride, k_stride, v_stride, o_stride};
   for (int i = 0; i < rank; ++i) {
     pl->shape[i] = shape[i];
@@ -698,6 +748,23 @@ sdpa_status sdpa_plan_set_lse(sdpa_plan* plan, float* lse, const int64_t* lse_st
 }
 
 void sdpa_plan_destroy(sdpa_plan* plan) { delete plan; }
+
+sdpa_status sdpa_mask_tiles(const uint8_t* mask, int64_t L, void* tile_bits,
+                            uint8_t* tile_class, void* stream) {
+  if (!mask || !tile_bits || !tile_class) return SDPA_ERR_NULL;
+  if (L < 1 || (L + 127) / 128 > 65535) return SDPA_ERR_SHAPE;
+  if (!aligned16(tile_bits)) return SDPA_ERR_LAYOUT;
+  sdpa_impl::MaskTilesParams mt{};
+  mt.mask = mask;
+  mt.L = static_cast<int>(L);
+  mt.n_tiles = static_cast<int>((L + 127) / 128);
+  mt.vec16 = (L % 16) == 0 && aligned16(mask);
+  mt.bits = static_cast<uint16_t*>(tile_bits);
+  mt.tile_class = tile_class;
+  return sdpa_impl::launch_mask_tiles(mt, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? SDPA_OK
+             : SDPA_ERR_CUDA;
+}
 
 const char* sdpa_status_string(sdpa_status status) {
   switch (status) {

@@ -370,6 +370,59 @@ __device__ __forceinline__ bool dense_next(const sdpa_impl::FwdParams& p, DenseI
   return false;
 }
 
+// Explicit mask with a tile summary: a job visits every key tile except
+// those whose every entry is removed for both of its query tiles.  Bit i of
+// the result: key tile 32 * chunk + i is visited (one ballot per 32 tiles;
+// every lane of the warp takes part).
+__device__ __forceinline__ uint32_t visit_chunk(const sdpa_impl::FwdParams& p, const Work& w,
+                                                int chunk) {
+  const int kt = chunk * 32 + static_cast<int>(threadIdx.x & 31);
+  bool visit = false;
+  if (kt < p.n_tiles) {
+#pragma unroll
+    for (int t = 0; t < kTilesPerCta; ++t)
+      visit = visit || (w.tile[t] < p.n_tiles &&
+                        __ldg(p.tile_class + static_cast<int64_t>(w.tile[t]) * p.n_tiles + kt) !=
+                            sdpa_impl::kTileRemoved);
+  }
+  return __ballot_sync(0xffffffffu, visit);
+}
+
+// n_kv of each present tile (and n_kv_max) becomes the number of visited key
+// tiles.  A job that visits none keeps n_kv = 0 for both tiles: the MMA and
+// load roles skip it and the softmax writes its rows as zeros.
+__device__ __forceinline__ void count_visits(const sdpa_impl::FwdParams& p, Work& w) {
+  int n = 0;
+  for (int c = 0; c * 32 < p.n_tiles; ++c) n += __popc(visit_chunk(p, w, c));
+#pragma unroll
+  for (int t = 0; t < kTilesPerCta; ++t) w.n_kv[t] = (w.n_kv[t] > 0) ? n : 0;
+  w.n_kv_max = n;
+}
+
+// The visited key tiles of one job in increasing order, one per call.
+struct KeyTileCursor {
+  int chunk;
+  uint32_t bits;  // visited tiles of `chunk` not yet returned
+};
+
+// Key tile of the j-th step of a job: j itself, or with a tile summary the
+// next visited tile (the cursor is called exactly n_kv_max times per job).
+template <int MODE>
+__device__ __forceinline__ int next_key_tile(const sdpa_impl::FwdParams& p, const Work& w,
+                                             KeyTileCursor& c, int j) {
+  if constexpr (MODE != sdpa_impl::kMaskExplicit) {
+    return j;
+  } else {
+    if (p.tile_class == nullptr) return j;
+    const int last = (p.n_tiles - 1) >> 5;
+    while (c.bits == 0u && c.chunk < last) c.bits = visit_chunk(p, w, ++c.chunk);
+    if (c.bits == 0u) return p.n_tiles - 1;  // not reached: n_kv_max tiles exist
+    const int kt = c.chunk * 32 + __ffs(static_cast<int>(c.bits)) - 1;
+    c.bits &= c.bits - 1u;
+    return kt;
+  }
+}
+
 // Calls f(work) for every job of this CTA, in order; stops when f returns
 // false.  VARLEN: packed sequences described by p.cu_seqlens.
 template <int MODE, bool VARLEN, typename F>
@@ -377,8 +430,11 @@ __device__ __forceinline__ void for_each_job(const sdpa_impl::FwdParams& p, F&& 
   if constexpr (!VARLEN) {
     DenseIter it{static_cast<int>(blockIdx.x), 0, 0};
     Work w;
-    while (dense_next<MODE>(p, it, w))
+    while (dense_next<MODE>(p, it, w)) {
+      if constexpr (MODE == sdpa_impl::kMaskExplicit)
+        if (p.tile_class != nullptr) count_visits(p, w);
       if (!f(w)) return;
+    }
   } else {
     const int step = static_cast<int>(gridDim.x);
     const int lane = static_cast<int>(threadIdx.x & 31);
@@ -418,9 +474,26 @@ __device__ __forceinline__ bool softmax_job(const sdpa_impl::FwdParams& p, const
                                             Barriers* bars, uint32_t tmem, int wq, int lane,
                                             SoftmaxCounters& cnt) {
   const int n = t ? w.n_kv[1] : w.n_kv[0];
-  if (n == 0) return true;
-  const uint64_t limit = p.wait_limit_ns;
   const int qt = t ? w.tile[1] : w.tile[0];
+  if (n == 0) {
+    if constexpr (MODE == sdpa_impl::kMaskExplicit) {
+      // A present tile whose job visits no key tile: every key of every
+      // row is removed, so the rows are zeros (and log-sum-exp -inf).
+      const int row_z = qt * kBlockM + wq * 32 + lane;
+      if (p.tile_class != nullptr && qt < p.n_tiles && row_z < w.len) {
+        if (p.lse != nullptr)
+          p.lse[w.batch * p.lse_sb + w.head * p.lse_sh +
+                static_cast<int64_t>(w.row0 + row_z) * p.lse_sl] = -INFINITY;
+        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(p.out) +
+                                              w.batch * p.o_sb + w.head * p.o_sh +
+                                              static_cast<int64_t>(w.row0 + row_z) * p.o_sl);
+#pragma unroll
+        for (int v = 0; v < D / 8; ++v) dst[v] = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+    return true;
+  }
+  const uint64_t limit = p.wait_limit_ns;
   using Plan = TmemPlan<D>;
   const uint32_t tS_base = tmem + (t ? Plan::s_col(1) : Plan::s_col(0));
   const uint32_t tO_base = tmem + (t ? Plan::o_col(1) : Plan::o_col(0));
@@ -437,9 +510,25 @@ __device__ __forceinline__ bool softmax_job(const sdpa_impl::FwdParams& p, const
   float m_used = -INFINITY;  // running max actually used in the exponentials
   float l = 0.0f;            // running row sum of probabilities
   bool ok = true;
+  KeyTileCursor kc{-1, 0u};
+  // With a tile summary the next visited tile and this row's 128 bits of it
+  // are fetched one tile ahead, so the load's latency overlaps a whole tile
+  // of work instead of the wait for S.  (A tile that removes nothing has
+  // zero bits and skips the select below.)
+  int kt_next = next_key_tile<MODE>(p, w, kc, 0);
+  uint4 bits_next = make_uint4(0u, 0u, 0u, 0u);
+  const uint4* tile_bits_row = nullptr;
+  if constexpr (MODE == sdpa_impl::kMaskExplicit) {
+    if (p.tile_class != nullptr) {
+      tile_bits_row = p.tile_bits + static_cast<int64_t>(qt) * p.n_tiles * kBlockM + r;
+      bits_next = __ldg(tile_bits_row + static_cast<int64_t>(kt_next) * kBlockM);
+    }
+  }
 
   for (int j = 0; j < n; ++j) {
-    const int col0 = j * kBlockN;
+    const int kt = kt_next;
+    if (tile_bits_row == nullptr) kt_next = j + 1;  // every key tile in order
+    const int col0 = kt * kBlockN;
     const bool tail = col0 + kBlockN > w.len;
     bool masked_tile = tail || (MODE == sdpa_impl::kMaskCausal && j == qt);
     // Explicit mask: this row's 128 mask bytes for tile j, one bit per key
@@ -449,7 +538,18 @@ __device__ __forceinline__ bool softmax_job(const sdpa_impl::FwdParams& p, const
     if constexpr (MODE == sdpa_impl::kMaskExplicit) {
       const bool row_ok = row_g < w.len;
       const uint8_t* mrow = p.mask + static_cast<int64_t>(row_ok ? row_g : 0) * p.L + col0;
-      if (p.mask_vec16 && !tail && row_g - lane + 31 < w.len) {
+      if (tile_bits_row != nullptr) {
+        // Tile summary: the bits fetched during the previous tile (a warp
+        // reads 512 contiguous bytes), and the next tile's now.
+        mbits[0] = bits_next.x;
+        mbits[1] = bits_next.y;
+        mbits[2] = bits_next.z;
+        mbits[3] = bits_next.w;
+        if (j + 1 < n) {
+          kt_next = next_key_tile<MODE>(p, w, kc, j + 1);
+          bits_next = __ldg(tile_bits_row + static_cast<int64_t>(kt_next) * kBlockM);
+        }
+      } else if (p.mask_vec16 && !tail && row_g - lane + 31 < w.len) {
         static_assert(kBlockN == 128, "the mask transpose assumes 128-key tiles");
         // Coalesced: lane (g, c) = (lane / 8, lane % 8) reads 16 bytes of
         // row 8g + i at keys 16c.. for i = 0..7, so each load instruction
@@ -795,6 +895,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // whose Q was loaded; a give-up drains what was issued.
     int g = 0, k_end = 0, v_end = 0, jobs = 0;
     for_each_job<MODE, VARLEN>(p, [&](const Work& w) -> bool {
+      if (w.n_kv_max == 0) return true;  // masked out entirely: nothing to load
       // The previous job's Q must be consumed (all its S products done).
       if (jobs > 0 && !warp_wait_phase(&bars->q_empty, (jobs - 1) & 1, bars, limit, kSiteEmpty))
         return false;
@@ -808,7 +909,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                      c * 64, w.row0 + w.tile[t] * kBlockM, w.head, w.batch, p.pos_q);
       }
       ++jobs;
-      for (int j = 0; j < w.n_kv_max; ++j, ++g) {
+      // Key tiles in order; with a mask summary every tile is examined and
+      // the ones the job does not visit are passed over.
+      const bool summary = MODE == sdpa_impl::kMaskExplicit && p.tile_class != nullptr;
+      const int n_scan = summary ? p.n_tiles : w.n_kv_max;
+      uint32_t visit = 0xffffffffu;
+      for (int kt = 0; kt < n_scan; ++kt) {
+        if (summary) {
+          if ((kt & 31) == 0) visit = visit_chunk(p, w, kt >> 5);
+          if (((visit >> (kt & 31)) & 1u) == 0u) continue;
+        }
         const int s = g % Lay::kKStages;
         const int use = g / Lay::kKStages;
         if (use > 0 &&
@@ -819,7 +929,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c = 0; c < Lay::kChunks; ++c)
             tma_tile(sK + s * Lay::kTileBytes + c * Lay::kChunkBytes, &p.tm_k, &bars->k_full[s],
-                     c * 64, w.row0 + j * kBlockN, w.head, w.batch, p.pos_k);
+                     c * 64, w.row0 + kt * kBlockN, w.head, w.batch, p.pos_k);
         }
         k_end = g + 1;
         const int sv = g % Lay::kVStages;
@@ -832,9 +942,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c = 0; c < Lay::kChunks; ++c)
             tma_tile(sV + sv * Lay::kTileBytes + c * Lay::kChunkBytes, &p.tm_v, &bars->v_full[sv],
-                     c * 64, w.row0 + j * kBlockN, w.head, w.batch, p.pos_v);
+                     c * 64, w.row0 + kt * kBlockN, w.head, w.batch, p.pos_v);
         }
         v_end = g + 1;
+        ++g;
       }
       return true;
     });
@@ -897,6 +1008,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t p_seen[kTilesPerCta] = {0, 0}, t_jobs[kTilesPerCta] = {0, 0};
     uint32_t f_seen[kTilesPerCta] = {0, 0};
     for_each_job<MODE, VARLEN>(p, [&](const Work& w) -> bool {
+      if (w.n_kv_max == 0) return true;  // masked out entirely: no products
       if (!warp_wait_phase(&bars->q_full, jobs & 1, bars, limit, kSiteQFull) ||
           !warp_wait_phase(&bars->k_full[g % Lay::kKStages], (g / Lay::kKStages) & 1, bars, limit,
                            kSiteKFull))
@@ -1097,6 +1209,53 @@ cudaError_t launch_mode(const sdpa_impl::FwdParams& p, int mode, int max_ctas,
   }
 }
 
+// Mask summary: CTA (kt, qt) reads 128 x 128 tile of the byte mask once
+// (16-byte loads, eight threads per 128-byte row segment), writes its rows
+// as bits (keys and rows past L as removed) and classifies the tile by the
+// entries inside [L, L].
+__global__ void __launch_bounds__(256) mask_tiles_kernel(const sdpa_impl::MaskTilesParams p) {
+  grid_dependency_wait();
+  grid_launch_dependents();
+  const int kt = static_cast<int>(blockIdx.x), qt = static_cast<int>(blockIdx.y);
+  const int tid = static_cast<int>(threadIdx.x);
+  const int col = kt * kBlockN + 16 * (tid & 7);
+  uint16_t* dst = p.bits + (static_cast<int64_t>(qt) * p.n_tiles + kt) * (kBlockM * 8);
+  bool any_removed = false, any_kept = false;
+#pragma unroll
+  for (int i = 0; i < kBlockM / 32; ++i) {
+    const int r = i * 32 + (tid >> 3);
+    const int row = qt * kBlockM + r;
+    uint32_t bits = 0xffffu;
+    if (row < p.L) {
+      const uint8_t* src = p.mask + static_cast<int64_t>(row) * p.L + col;
+      if (p.vec16 && col + 16 <= p.L) {
+        const uint4 x = __ldg(reinterpret_cast<const uint4*>(src));
+        bits = nonzero_byte_bits(x.x) | (nonzero_byte_bits(x.y) << 4) |
+               (nonzero_byte_bits(x.z) << 8) | (nonzero_byte_bits(x.w) << 12);
+        any_removed = any_removed || bits != 0u;
+        any_kept = any_kept || bits != 0xffffu;
+      } else {
+        bits = 0u;
+        for (int b = 0; b < 16; ++b) {
+          const bool in = col + b < p.L;
+          const bool removed = !in || __ldg(src + b) != 0;
+          bits |= (removed ? 1u : 0u) << b;
+          if (in) {
+            any_removed = any_removed || removed;
+            any_kept = any_kept || !removed;
+          }
+        }
+      }
+    }
+    dst[r * 8 + (tid & 7)] = static_cast<uint16_t>(bits);
+  }
+  const int removed = __syncthreads_or(any_removed ? 1 : 0);
+  const int kept = __syncthreads_or(any_kept ? 1 : 0);
+  if (tid == 0)
+    p.tile_class[static_cast<int64_t>(qt) * p.n_tiles + kt] =
+        !removed ? sdpa_impl::kTileKept : (!kept ? sdpa_impl::kTileRemoved : sdpa_impl::kTileMixed);
+}
+
 // Test hook: y = 2^x through the FMA-pipe polynomial (pairs of elements).
 __global__ void exp2_poly_kernel(const float* x, float* y, int64_t n) {
   const int64_t i = 2 * (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x);
@@ -1122,6 +1281,21 @@ cudaError_t launch_exp2_poly(const float* x, float* y, int64_t n, cudaStream_t s
   const unsigned blocks = static_cast<unsigned>((pairs + 255) / 256);
   exp2_poly_kernel<<<blocks, 256, 0, stream>>>(x, y, n);
   return cudaGetLastError();
+}
+
+cudaError_t launch_mask_tiles(const MaskTilesParams& p, cudaStream_t stream) {
+  if (p.n_tiles < 1 || p.n_tiles > 65535) return cudaErrorInvalidValue;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(p.n_tiles), static_cast<unsigned>(p.n_tiles), 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, mask_tiles_kernel, p);
 }
 
 cudaError_t launch_forward(const FwdParams& p, int head_dim, int mask_mode, bool bf16,

@@ -29,8 +29,28 @@ struct FwdParams {
   float scale_log2;     // scale * log2(e)
   int pos_q[3], pos_k[3], pos_v[3];  // tensor-map coordinate slot (1..3) of L, H, B
   int mask_vec16;       // 1: mask rows may be read as 16-byte vectors (L % 16 == 0, aligned)
+  // Optional tile summary of the explicit mask (both null: read the mask
+  // bytes).  Tile (qt, kt) of the n_tiles x n_tiles grid of 128 x 128 tiles:
+  // class byte tile_class[qt * n_tiles + kt] (kTileKept / kTileMixed /
+  // kTileRemoved) and 128 rows of 128 bits at tile_bits[(qt * n_tiles + kt) *
+  // 128 + row] (bit c of word w = key 32w + c removed; keys and rows past L
+  // read as removed).
+  const uint4* tile_bits;
+  const uint8_t* tile_class;
   int debug_withhold_q; // test hook: 1 = never load Q, so every consumer wait runs out
   uint64_t wait_limit_ns;  // bound on any single barrier wait
+};
+
+// Tile classes of a mask summary, counting only entries inside [L, L].
+enum TileClass : uint8_t { kTileKept = 0, kTileMixed = 1, kTileRemoved = 2 };
+
+// Mask summary: one CTA per 128 x 128 tile of an [L, L] byte mask.
+struct MaskTilesParams {
+  const uint8_t* mask;  // [L, L] row-major, nonzero = removed
+  int L, n_tiles;
+  int vec16;            // rows may be read as 16-byte vectors
+  uint16_t* bits;       // [n_tiles^2][128 rows][8] 16-bit words (the tile_bits layout)
+  uint8_t* tile_class;  // [n_tiles^2]
 };
 
 // Sparse top-k attention: query row i (all heads of head group g) attends to
@@ -81,6 +101,10 @@ cudaError_t launch_forward(const FwdParams& p, int head_dim, int mask_mode, bool
                            int max_ctas, cudaStream_t stream);
 
 // Test hook: y[i] = 2^x[i] through the kernel's FMA-pipe polynomial.
+// Writes the tile summary of p.mask (PDL launch: waits for the previous
+// kernel in the stream before reading the mask).
+cudaError_t launch_mask_tiles(const MaskTilesParams& p, cudaStream_t stream);
+
 cudaError_t launch_exp2_poly(const float* x, float* y, int64_t n, cudaStream_t stream);
 
 // Reads and clears the device status word (nonzero = a barrier wait timed out).
