@@ -158,6 +158,41 @@ SDPA_API sdpa_status sdpa_plan_launch(const sdpa_plan* plan, void* stream);
 SDPA_API void sdpa_plan_destroy(sdpa_plan* plan);
 
 /*
+ * sdpa_forward_masked_noalloc -- a masked forward that allocates nothing.
+ *
+ * The pages have no counterpart: this entry point is for callers that
+ * cannot allocate device memory -- code that runs inside another runtime
+ * whose memory pool has already reserved the device's memory, or a serving
+ * loop that must not call cudaMalloc/cudaFree (they can synchronise the
+ * whole device) -- but still want the masked fast path that a masked plan
+ * gets from its summary buffer.  Here the mask summary (see sdpa_mask_tiles)
+ * lives in one fixed array inside the library instead: 2,098,176 bytes of
+ * device memory on every GPU that loads the library, held until the process
+ * exits, enough for L <= SDPA_NOALLOC_MAX_L.
+ *
+ * Arguments as sdpa_forward with an explicit mask (no is_causal): mask must
+ * be non-NULL (else SDPA_ERR_NULL); L > SDPA_NOALLOC_MAX_L returns
+ * SDPA_ERR_SHAPE, the scratch array's limit; other errors as sdpa_forward.
+ * The caller passes and owns q, k, v, out and mask; the call allocates no
+ * device or pinned memory.  The first call on a device looks up the array's
+ * device address on that device (it must be current, as for every call) and
+ * caches it; make that first call before any stream capture.  Every call
+ * on a device uses the same array and leaves its last summary in it:
+ * nothing there needs to start at zero, because each call rewrites every
+ * byte it then reads, but calls whose work overlaps on the GPU (different
+ * streams, or different threads) race on the array and must be ordered by
+ * the caller.
+ */
+#define SDPA_NOALLOC_MAX_L 4096
+SDPA_API sdpa_status sdpa_forward_masked_noalloc(const void* q, const void* k, const void* v,
+                                                 void* out, sdpa_dtype dtype, int rank,
+                                                 const int64_t* shape, const int64_t* q_stride,
+                                                 const int64_t* k_stride,
+                                                 const int64_t* v_stride,
+                                                 const int64_t* o_stride, const uint8_t* mask,
+                                                 float scale, void* stream);
+
+/*
  * sdpa_mask_tiles -- the tile summary of an explicit mask (the mask-tile
  * skip bitmap masked plans use), written into caller-owned memory.
  *

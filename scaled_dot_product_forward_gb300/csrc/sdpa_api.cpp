@@ -406,6 +406,25 @@ sdpa_status sdpa_forward(const void* q, const void* k, const void* v, void* out,
   return launch_prepared(pr, stream);
 }
 
+sdpa_status sdpa_forward_masked_noalloc(const void* q, const void* k, const void* v, void* out,
+                                        sdpa_dtype dtype, int rank, const int64_t* shape,
+                                        const int64_t* q_stride, const int64_t* k_stride,
+                                        const int64_t* v_stride, const int64_t* o_stride,
+                                        const uint8_t* mask, float scale, void* stream) {
+  if (!mask) return SDPA_ERR_NULL;
+  Prepared pr;
+  const sdpa_status s = build_params(q, k, v, out, dtype, rank, shape, q_stride, k_stride,
+                                     v_stride, o_stride, 0, mask, scale, &pr);
+  if (s != SDPA_OK) return s;
+  if (pr.p.L > SDPA_NOALLOC_MAX_L) return SDPA_ERR_SHAPE;  // beyond the fixed scratch
+  const uint4* bits = nullptr;
+  const uint8_t* cls = nullptr;
+  if (sdpa_impl::noalloc_mask_tiles(pr.device, &bits, &cls) != cudaSuccess) return SDPA_ERR_CUDA;
+  pr.p.tile_bits = bits;
+  pr.p.tile_class = cls;
+  return launch_prepared(pr, stream);
+}
+
 sdpa_status sdpa_forward_lse(const void* q, const void* k, const void* v, void* out, float* lse,
                              sdpa_dtype dtype, int rank, const int64_t* shape,
                              const int64_t* q_stride, const int64_t* k_stride,

@@ -37,6 +37,7 @@
 // drains what it already issued and frees its tensor memory.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <mutex>
 
 #include "ptx.cuh"
 #include "sdpa_internal.h"
@@ -46,6 +47,16 @@ using namespace sdpa_dev;
 // Device status word: bit 0 = some barrier wait ran out of time; the upper
 // bits name the wait site.  Read and cleared by sdpa_last_device_status().
 __device__ unsigned int g_sdpa_device_status = 0;
+
+// Mask-summary scratch of sdpa_forward_masked_noalloc, for callers that
+// cannot allocate device memory: the row bits of up to 32 x 32 tiles (an
+// [L, L] mask with L <= 4096), then their class bytes at a fixed offset.
+// A file-scope array, so every GPU that loads the library holds these
+// 2,098,176 bytes until the process exits; host code gets its device
+// address with cudaGetSymbolAddress (sdpa_impl::noalloc_mask_tiles).
+static __device__ __align__(256) uint8_t
+    g_noalloc_mask_tiles[sdpa_impl::kNoAllocMaxTiles * sdpa_impl::kNoAllocMaxTiles *
+                         (128 * 16 + 1)];
 
 namespace {
 
@@ -1306,6 +1317,30 @@ cudaError_t launch_forward(const FwdParams& p, int head_dim, int mask_mode, bool
                 : launch_mode<64, false>(p, mask_mode, max_ctas, stream);
   return bf16 ? launch_mode<128, true>(p, mask_mode, max_ctas, stream)
               : launch_mode<128, false>(p, mask_mode, max_ctas, stream);
+}
+
+cudaError_t noalloc_mask_tiles(int device, const uint4** tile_bits,
+                               const uint8_t** tile_class) {
+  // One cached device address per device, found the first time a device
+  // asks (with that device current, as cudaGetSymbolAddress requires).
+  static std::mutex mu;
+  static void* addr[kNoAllocMaxDevices] = {};
+  if (device < 0 || device >= kNoAllocMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[device] == nullptr) {
+    int cur = -1;
+    cudaError_t e = cudaGetDevice(&cur);
+    if (e != cudaSuccess) return e;
+    if (cur != device) return cudaErrorInvalidDevice;
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_noalloc_mask_tiles);
+    if (e != cudaSuccess) return e;
+    addr[device] = ptr;
+  }
+  *tile_bits = static_cast<const uint4*>(addr[device]);
+  *tile_class = static_cast<const uint8_t*>(addr[device]) +
+                static_cast<size_t>(kNoAllocMaxTiles) * kNoAllocMaxTiles * kBlockM * 16;
+  return cudaSuccess;
 }
 
 cudaError_t read_and_clear_device_status(cudaStream_t stream, unsigned int* status) {

@@ -105,6 +105,14 @@ cudaError_t launch_forward(const FwdParams& p, int head_dim, int mask_mode, bool
 // kernel in the stream before reading the mask).
 cudaError_t launch_mask_tiles(const MaskTilesParams& p, cudaStream_t stream);
 
+// sdpa_forward_masked_noalloc: the mask summary lives in a fixed array in
+// the library, enough for n_tiles <= kNoAllocMaxTiles.  Returns the device
+// addresses of its bits and class parts for `device`, which must be current
+// (looked up once per device with cudaGetSymbolAddress, then cached).
+constexpr int kNoAllocMaxTiles = 32;
+constexpr int kNoAllocMaxDevices = 64;
+cudaError_t noalloc_mask_tiles(int device, const uint4** tile_bits, const uint8_t** tile_class);
+
 cudaError_t launch_exp2_poly(const float* x, float* y, int64_t n, cudaStream_t stream);
 
 // Reads and clears the device status word (nonzero = a barrier wait timed out).
