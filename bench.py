@@ -559,7 +559,9 @@ def main(argv=None):
     mean_launch_ms = statistics.fmean(r["per_launch_ms"])
     achieved = r["flops"] / (mean_launch_ms * 1e-3) / 1e12
     peak, _, peak_kind = load_peaks()
-    traffic = load_traffic(args.workload)
+    # A masked plan runs the mask-summary path (its own ncu capture).
+    summary = (args.plan or args.graph) and w.p_masked is not None
+    traffic = load_traffic(f"{args.workload}plan" if summary else args.workload)
     e2e_ms = max_over_ranks(r["e2e_ms"], world)
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
