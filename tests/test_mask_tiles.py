@@ -126,3 +126,43 @@ def test_masked_workload_plan_sampled(sdpa_lib):
     plan.close()
     assert torch.equal(out, sdpa_lib.sdpa_forward(qd, kd, vd, mask=md))
     assert torch.all(out[:, :, sdpa_inputs.full_rows(w)] == 0)
+
+
+def test_masked_plan_rank3_unaligned_length(sdpa_lib):
+    """Rank-3 [H, L, D] with L = 300: the mask rows are not 16-byte multiples,
+    so the summary kernel reads bytes one at a time, and the last tiles are
+    ragged in both rows and keys."""
+    L, D = 300, 64
+    i = torch.arange(L)
+    mask = ((i[:, None] - i[None, :]).abs() >= 90).to(torch.uint8)
+    mask[:40] = 1                                   # rows with every key removed
+    q, k, v = sdpa_inputs.custom((3, L, D), dtype=torch.bfloat16, seed=77)
+    qd, kd, vd, md = (x.cuda() for x in (q, k, v, mask))
+    out = torch.full_like(qd, float("nan"))
+    plan = sdpa_lib.SdpaPlan(qd, kd, vd, out, mask=md)
+    plan.launch()
+    torch.cuda.synchronize()
+    plan.close()
+    assert sdpa_lib.sdpa_last_device_status()[0] == 0
+    assert torch.equal(out, sdpa_lib.sdpa_forward(qd, kd, vd, mask=md))
+    assert torch.all(out[:, :40] == 0)
+    check(out.double().cpu().numpy(), oracle.sdpa(q, k, v, mask=mask), "rank-3 L=300")
+
+
+def test_masked_plan_rebinds_to_another_mask(sdpa_lib):
+    """set_pointers moves a masked plan to another mask buffer: its summary
+    is rebuilt from the new mask on the next launch."""
+    L, D = 512, 128
+    q, k, v = sdpa_inputs.custom((1, 2, L, D), dtype=torch.bfloat16, seed=78)
+    qd, kd, vd = (x.cuda() for x in (q, k, v))
+    m1, m2 = masks(L)["blockdiag"].cuda(), masks(L)["dead_rows"].cuda()
+    out = torch.empty_like(qd)
+    plan = sdpa_lib.SdpaPlan(qd, kd, vd, out, mask=m1)
+    plan.launch()
+    first = out.clone()
+    plan.set_pointers(qd, kd, vd, out, mask=m2)
+    plan.launch()
+    torch.cuda.synchronize()
+    plan.close()
+    assert torch.equal(first, sdpa_lib.sdpa_forward(qd, kd, vd, mask=m1))
+    assert torch.equal(out, sdpa_lib.sdpa_forward(qd, kd, vd, mask=m2))
