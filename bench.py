@@ -16,7 +16,11 @@ e2e          the same metric through the same C-ABI call, with pinned host
              buffer sets and three streams (copy-in, compute, copy-out).
 roofline     achieved = algorithmic FLOPs per launch / mean per-launch kernel
              time (CUDA events around each launch in the timed region); peak =
-             the measured dense bf16 GEMM rate (burst) of this GPU model.
+             the measured dense bf16 GEMM rate (burst) of this GPU model.  A
+             workload whose algorithmic FLOP per byte is below the ridge of
+             the measured peaks (the rank-3 and [8,16,1024,64] cases) is
+             reported against HBM instead: GB/s of algorithmic bytes against
+             the measured copy bandwidth.
 cpu_baseline the fp64 oracle on the host cores, on a bounded sample of query
              rows of the same workload, in the same unit.
 """
@@ -62,6 +66,27 @@ def load_peaks():
         return float(pk["bf16_tflops"]), float(pk.get("hbm_gbs", 0.0)), "measured"
     except (OSError, KeyError, ValueError):
         return FALLBACK_BF16_TFLOPS, 6800.0, "fallback"
+
+
+def roofline_of(w, flops, mean_launch_ms, peak, hbm_peak, peak_kind, traffic):
+    """The bound a workload's arithmetic intensity puts it under at the
+    measured peaks: the tensor core (TFLOP/s against the bf16 GEMM rate) when
+    its algorithmic FLOP per algorithmic byte is at or above the ridge, else
+    HBM (GB/s of algorithmic bytes against the measured copy bandwidth)."""
+    alg_bytes = w.alg_bytes()
+    tflops = flops / (mean_launch_ms * 1e-3) / 1e12
+    gbs = alg_bytes / (mean_launch_ms * 1e-3) / 1e9
+    ridge = peak * 1e12 / (hbm_peak * 1e9) if hbm_peak > 0 else 0.0
+    common = {"traffic": traffic, "alg_flops_per_launch": flops,
+              "alg_bytes_per_launch": alg_bytes, "flop_per_byte": flops / alg_bytes,
+              "ridge_flop_per_byte": ridge, "mean_launch_ms": mean_launch_ms}
+    if hbm_peak > 0 and flops / alg_bytes < ridge:
+        return {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
+                "frac": gbs / hbm_peak, "peak_source": f"{peak_kind} HBM copy",
+                "tflops": tflops, **common}
+    return {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": UNIT,
+            "frac": tflops / peak, "peak_source": f"{peak_kind} dense bf16 (burst)",
+            "gbs": gbs, **common}
 
 
 def load_traffic(workload_id, sources=None):
@@ -557,8 +582,7 @@ def main(argv=None):
     ms_per_step = total_ms / args.steps
     value = world * r["flops"] / (ms_per_step * 1e-3) / 1e12
     mean_launch_ms = statistics.fmean(r["per_launch_ms"])
-    achieved = r["flops"] / (mean_launch_ms * 1e-3) / 1e12
-    peak, _, peak_kind = load_peaks()
+    peak, hbm_peak, peak_kind = load_peaks()
     # A masked plan runs the mask-summary path (its own ncu capture).
     summary = (args.plan or args.graph) and w.p_masked is not None
     traffic = load_traffic(f"{args.workload}plan" if summary else args.workload)
@@ -567,12 +591,8 @@ def main(argv=None):
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": dtype, "data": "synthetic",
             "config": config,
-            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
-                         "unit": UNIT, "frac": achieved / peak,
-                         "peak_source": f"{peak_kind} dense bf16 (burst)",
-                         "traffic": traffic,
-                         "alg_flops_per_launch": r["flops"],
-                         "mean_launch_ms": mean_launch_ms},
+            "roofline": roofline_of(w, r["flops"], mean_launch_ms, peak, hbm_peak, peak_kind,
+                                    traffic),
             "e2e": {"value": world * r["flops"] / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
                     "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"],
                     "ms_per_step": e2e_ms},
