@@ -166,3 +166,33 @@ def test_masked_plan_rebinds_to_another_mask(sdpa_lib):
     plan.close()
     assert torch.equal(first, sdpa_lib.sdpa_forward(qd, kd, vd, mask=m1))
     assert torch.equal(out, sdpa_lib.sdpa_forward(qd, kd, vd, mask=m2))
+
+
+def test_masked_plan_visits_across_chunks(sdpa_lib):
+    """L = 4224: 33 key tiles, so the visited-tile cursor spans two 32-tile
+    chunks, with skipped tiles on both sides of the chunk edge and a job in
+    the second chunk that visits nothing."""
+    L, D = 4224, 64
+    i = torch.arange(L)
+    mask = ((i[:, None] - i[None, :]).abs() >= 300).to(torch.uint8)
+    mask[4096:] = 1                                  # the last query tile removes every key
+    q, k, v = sdpa_inputs.custom((1, 2, L, D), dtype=torch.float16, seed=79)
+    qd, kd, vd, md = (x.cuda() for x in (q, k, v, mask))
+    bits, cls = summary_of(sdpa_lib, mask)
+    assert cls.shape == (33, 33) and (cls == 2).sum() > 0 and cls[32].tolist() == [2] * 33
+    out = torch.empty_like(qd)
+    plan = sdpa_lib.SdpaPlan(qd, kd, vd, out, mask=md)
+    plan.launch()
+    torch.cuda.synchronize()
+    plan.close()
+    assert sdpa_lib.sdpa_last_device_status()[0] == 0
+    assert torch.equal(out, sdpa_lib.sdpa_forward(qd, kd, vd, mask=md))
+    assert torch.all(out[:, :, 4096:] == 0)
+    g = torch.Generator().manual_seed(80)
+    rows = torch.stack([torch.zeros(96, dtype=torch.long), torch.randint(0, 2, (96,), generator=g),
+                        torch.randint(0, L, (96,), generator=g)], 1)
+    edge = torch.tensor([[0, 1, r] for r in (0, 4095, 4096, 4223, 3967, 3968)])
+    rows = torch.cat([rows, edge])
+    ref = oracle.sdpa_rows(q, k, v, rows.numpy(), mask=mask)
+    got = out[rows[:, 0], rows[:, 1], rows[:, 2]].double().cpu().numpy()
+    check(got, ref, "33 tiles")

@@ -189,3 +189,20 @@ def test_structured_masks(sdpa_lib, kind):
         mask = torch.zeros(L, L, dtype=torch.bool)
     out = run(sdpa_lib, q, k, v, mask=mask)
     check(out.double().cpu().numpy(), oracle.sdpa(q, k, v, mask=mask), kind)
+
+
+def test_long_sequence_sampled(sdpa_lib):
+    """A 131072-long causal sequence: row and tile indices far past 2^16 and
+    an L*L far past 2^31, checked on sampled rows (every tile edge would be
+    too many for the fp64 oracle)."""
+    L, D = 131072, 64
+    q, k, v = sdpa_inputs.custom((1, 2, L, D), dtype=torch.bfloat16, seed=81)
+    out = run(sdpa_lib, q, k, v, is_causal=True)
+    g = torch.Generator().manual_seed(82)
+    rows = torch.stack([torch.zeros(40, dtype=torch.long), torch.randint(0, 2, (40,), generator=g),
+                        torch.randint(0, L, (40,), generator=g)], 1)
+    edge = torch.tensor([[0, h, r] for h in (0, 1) for r in (0, 127, 128, L - 129, L - 128, L - 1)])
+    rows = torch.cat([rows, edge])
+    ref = oracle.sdpa_rows(q, k, v, rows.numpy(), is_causal=True)
+    got = out.cpu()[rows[:, 0], rows[:, 1], rows[:, 2]].double().numpy()
+    check(got, ref, "L=131072")
