@@ -267,7 +267,9 @@ __device__ __forceinline__ bool job_tiles(int n_tiles, int k, int sub, Work& w) 
 // step.  Lane i holds sequence chunk + i (its start and length and the
 // inclusive count of units up to it within the chunk); `before` counts the
 // units of earlier chunks.  Units are numbered sequence by sequence, each
-// sequence's heads in order.  The offsets are used as the running maximum of
+// sequence's heads in order; with at most 32 sequences (one chunk) the
+// sequences are taken longest first, which spreads the costly units over
+// the CTAs before the cheap ones fill the gaps.  The offsets are used as the running maximum of
 // their values clamped to [0, total], so sequences never overlap and never
 // leave the buffers, whatever the array holds; for valid offsets (0 first,
 // nondecreasing, total last) that is the identity.  All 32 lanes run it.
@@ -293,6 +295,28 @@ __device__ __forceinline__ void cursor_load(const sdpa_impl::FwdParams& p, SeqCu
   c.start = st;
   c.len = e - st;
   c.carry_out = __shfl_sync(0xffffffffu, e, 31);
+  if (p.n_seqs <= 32) {
+    // Bitonic sort of the lanes by (length, then lower index) descending;
+    // the keys are distinct, so every warp of every CTA gets one order.
+    uint64_t key = (static_cast<uint64_t>(c.len) << 6) | static_cast<uint64_t>(31 - lane);
+    int s0 = c.start;
+#pragma unroll
+    for (int kb = 2; kb <= 32; kb <<= 1) {
+#pragma unroll
+      for (int jb = kb >> 1; jb > 0; jb >>= 1) {
+        const uint64_t ok = __shfl_xor_sync(0xffffffffu, key, jb);
+        const int os = __shfl_xor_sync(0xffffffffu, s0, jb);
+        // the lower lane of a pair keeps the larger key in a descending run
+        const bool take = (((lane & jb) == 0) == ((lane & kb) == 0)) ? (ok > key) : (ok < key);
+        if (take) {
+          key = ok;
+          s0 = os;
+        }
+      }
+    }
+    c.start = s0;
+    c.len = static_cast<int>(key >> 6);
+  }
   int incl = p.H * units_per_head(tiles_of(c.len));
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
