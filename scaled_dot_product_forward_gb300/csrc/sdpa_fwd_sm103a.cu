@@ -267,9 +267,11 @@ __device__ __forceinline__ bool job_tiles(int n_tiles, int k, int sub, Work& w) 
 // step.  Lane i holds sequence chunk + i (its start and length and the
 // inclusive count of units up to it within the chunk); `before` counts the
 // units of earlier chunks.  Units are numbered sequence by sequence, each
-// sequence's heads in order; with at most 32 sequences (one chunk) the
-// sequences are taken longest first, which spreads the costly units over
-// the CTAs before the cheap ones fill the gaps.  The offsets are used as the running maximum of
+// sequence's heads in order.  With at most 32 sequences (one chunk) the
+// order is by cost instead, since any unit can then be found in the chunk:
+// first every sequence's two-job units, longest sequence first, then the
+// one-job units (the middle pair of an odd pair count), longest first, so the
+// snake deals the costly units before the cheap ones fill the gaps.  The offsets are used as the running maximum of
 // their values clamped to [0, total], so sequences never overlap and never
 // leave the buffers, whatever the array holds; for valid offsets (0 first,
 // nondecreasing, total last) that is the identity.  All 32 lanes run it.
@@ -278,6 +280,7 @@ struct SeqCursor {
   int carry;      // running-maximum offset where this chunk starts
   int carry_out;  // ... and where it ends
   int start, len, incl;
+  int incl_half, full_units;  // one chunk only: inclusive one-job units, all two-job units
 };
 
 __device__ __forceinline__ void cursor_load(const sdpa_impl::FwdParams& p, SeqCursor& c,
@@ -316,6 +319,23 @@ __device__ __forceinline__ void cursor_load(const sdpa_impl::FwdParams& p, SeqCu
     }
     c.start = s0;
     c.len = static_cast<int>(key >> 6);
+    // two-job and one-job units of this sequence (per head: pairs / 2 and pairs % 2)
+    const int pairs = pairs_per_head(tiles_of(c.len));
+    int full = p.H * (pairs >> 1), half = p.H * (pairs & 1);
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int vf = __shfl_up_sync(0xffffffffu, full, off);
+      const int vh = __shfl_up_sync(0xffffffffu, half, off);
+      if (lane >= off) {
+        full += vf;
+        half += vh;
+      }
+    }
+    c.incl = full;
+    c.incl_half = half;
+    c.full_units = __shfl_sync(0xffffffffu, full, 31);
+    c.chunk_units = c.full_units + __shfl_sync(0xffffffffu, half, 31);
+    return;
   }
   int incl = p.H * units_per_head(tiles_of(c.len));
 #pragma unroll
@@ -338,6 +358,31 @@ __device__ __forceinline__ bool cursor_find(const sdpa_impl::FwdParams& p, SeqCu
     c.chunk += 32;
     c.carry = c.carry_out;
     cursor_load(p, c, lane);
+  }
+  if (p.n_seqs <= 32) {
+    // One chunk, ordered by cost: two-job units, then one-job units.
+    const bool half = u >= c.full_units;
+    const int rel = half ? u - c.full_units : u;
+    const unsigned hit = __ballot_sync(0xffffffffu, rel < (half ? c.incl_half : c.incl));
+    const int src = __ffs(static_cast<int>(hit)) - 1;
+    const int incl = __shfl_sync(0xffffffffu, half ? c.incl_half : c.incl, src);
+    const int len = __shfl_sync(0xffffffffu, c.len, src);
+    const int start = __shfl_sync(0xffffffffu, c.start, src);
+    n_tiles = tiles_of(len);
+    const int pairs = pairs_per_head(n_tiles);
+    w.batch = 0;
+    w.row0 = start;
+    w.len = len;
+    if (half) {
+      w.head = rel - (incl - p.H);  // one unit per head: the middle pair
+      k = pairs >> 1;
+    } else {
+      const int per_head = pairs >> 1;
+      const int r = rel - (incl - p.H * per_head);
+      w.head = r / per_head;
+      k = r - w.head * per_head;
+    }
+    return true;
   }
   const int rel = u - c.before;
   const unsigned hit = __ballot_sync(0xffffffffu, rel < c.incl);
