@@ -92,7 +92,7 @@ def roofline_of(w, flops, mean_launch_ms, peak, hbm_peak, peak_kind, traffic):
 def load_traffic(workload_id, sources=None):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
     on the current kernel source (else None).  ``workload_id`` is a dense
-    workload number or "sparse"."""
+    workload number, "varlen" or "sparse"."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
@@ -466,7 +466,8 @@ def extra_leg(args, path):
             "config": config,
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
                          "frac": achieved / peak, "peak_source": f"{peak_kind} dense bf16 (burst)",
-                         "traffic": load_traffic("sparse", SPARSE_SOURCES) if path == "sparse" else None,
+                         "traffic": (load_traffic("sparse", SPARSE_SOURCES) if path == "sparse"
+                                     else load_traffic("varlen")),
                          "alg_flops_per_launch": flops, "mean_launch_ms": ms},
             "e2e": {"value": flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
                     "h2d_bytes_per_step": sum(x.numel() * x.element_size() for x in ins),
