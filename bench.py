@@ -50,11 +50,23 @@ SPARSE_SOURCES = ["scaled_dot_product_forward_gb300/csrc/sdpa_sparse_sm103a.cu",
                   "scaled_dot_product_forward_gb300/csrc/ptx.cuh"]
 
 
+def code_of(text: str) -> str:
+    """A source file without its // comments and blank lines (the kernel
+    sources hold no '//' inside string literals and no block comments), so
+    that a comment edit keeps the identity of code that was profiled."""
+    lines = []
+    for line in text.splitlines():
+        code = line.split("//", 1)[0].rstrip()
+        if code:
+            lines.append(code)
+    return "\n".join(lines)
+
+
 def kernel_source_hash(sources=None) -> str:
     h = hashlib.sha256()
     for rel in sources or KERNEL_SOURCES:
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
+            h.update(code_of(f.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -9,26 +9,36 @@
 // HBM -- but built for Blackwell:
 //
 //   * persistent: at most one CTA per SM, each walking a static share of
-//     equal-cost units.  A job is a pair of adjacent 128-row query tiles
-//     (A = rows 256m.., B = rows 256m+128..) of one (batch, head); a unit is
-//     the causal pair P-1-k followed by pair k of the same head, so every
-//     unit costs the same number of key tiles.  Units are head-major, so the
-//     CTAs busy at one time share a few heads' K/V in L2.  The next job's Q
-//     load and first S products overlap the previous job's epilogue;
+//     the work.  A job is a pair of adjacent 128-row query tiles (A = rows
+//     256m.., B = rows 256m+128..) of one (batch, head); a unit is the causal
+//     pair P-1-k followed by pair k of the same head, so every unit costs the
+//     same number of key tiles.  Units are head-major, so the CTAs busy at
+//     one time share a few heads' K/V in L2.  Problems whose K and V fit in
+//     L2 deal jobs by falling cost in snake order over the CTAs instead;
+//     packed documents are found through a warp-wide cursor over cu_seqlens
+//     (and, with at most 32 of them, dealt by cost as well).  The next job's
+//     Q load and first S products overlap the previous job's epilogue;
 //   * warp 0 streams each job's Q_A, Q_B and one ring of K and V tiles that
 //     runs on across jobs, with TMA (128-byte swizzled boxes of 64 x 128
 //     elements), K and V with their own full/empty barriers;
-//   * warp 1 issues tcgen05.mma (one elected lane) in the order
+//   * warp 1 issues tcgen05.mma (one elected lane).  D = 128, in the order
 //       S_A(0) S_B(0) | PV_A(0) S_A(1) PV_B(0) S_B(1) | PV_A(1) S_A(2) ...
 //     so that while one softmax warpgroup works on its tile the tensor core
 //     is busy with the other tile's products; S = Q K^T lands in TMEM, and
-//     P (16-bit, written over S) is read from TMEM by O += P V;
+//     P (16-bit, written over S) is read from TMEM by O += P V.  D = 64 has
+//     room for P beside S, so S(j+1) of both tiles is issued as soon as the
+//     softmax has loaded S(j), ahead of PV(j);
 //   * warpgroup 1 owns tile A, warpgroup 2 tile B: one query row per thread
 //     (TMEM lane = row), so row max and row sum are in-thread tree
 //     reductions with no shuffles; scale, causal / explicit / ragged-tail
 //     masks and the online softmax happen in registers, O is rescaled in
 //     TMEM only when the running maximum grows by more than 2^8, and the
-//     epilogue writes O / l.
+//     epilogue writes O / l;
+//   * explicit masks: each row's 128 bits per key tile come either from the
+//     mask bytes (coalesced loads and an in-warp transpose) or, for masked
+//     plans, from a per-tile summary that mask_tiles_kernel writes before
+//     the forward; with the summary every role skips the key tiles that
+//     remove every key for both query tiles of its job.
 //
 // Safe softmax: a row with no admissible key ends with l = 0 and is written
 // as zeros, as the math backend's _safe_softmax does (same page, "Math

@@ -27,3 +27,11 @@ def test_bound_follows_arithmetic_intensity():
 def test_without_a_bandwidth_peak_everything_is_tensor_bound():
     w = sdpa_inputs.WORKLOADS[2]
     assert bench.roofline_of(w, w.flops(), 1.0, 1890.0, 0.0, "fallback", None)["bound"] == "tensor"
+
+
+def test_source_hash_ignores_comments_but_not_code():
+    a = "int f() {  // one\n  return 1;\n}\n"
+    b = "// a new header line\nint f() {  // two\n\n  return 1;\n}\n"
+    c = "int f() {\n  return 2;\n}\n"
+    assert bench.code_of(a) == bench.code_of(b)
+    assert bench.code_of(a) != bench.code_of(c)
