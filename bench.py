@@ -181,10 +181,12 @@ class ClockSampler:
 
 # --------------------------------------------------------- CPU (oracle) leg
 class OracleSampler:
-    """Times the fp64 oracle on random query rows of one head of workload
-    ``w`` (the operands are generated and widened once)."""
+    """Times the fp64 oracle on random query rows (b, h, i) of workload
+    ``w`` (the operands are generated and widened once).  The rows it
+    evaluates, and their oracle outputs, double as the parity sample of the
+    GPU output."""
 
-    def __init__(self, w):
+    def __init__(self, w, operands=None):
         import numpy as np
         import torch
 
@@ -192,13 +194,15 @@ class OracleSampler:
         import sdpa_inputs
 
         self.w = w
-        q, k, v, mask = sdpa_inputs.make(w)
+        q, k, v, mask = operands if operands is not None else sdpa_inputs.make(w)
         if w.rank == 3:
             q, k, v = q[None], k[None], v[None]
-        self.q, self.k, self.v = (x[:1, :1].to(torch.float64).numpy() for x in (q, k, v))
+        self.q, self.k, self.v = (x.to(torch.float64).numpy() for x in (q, k, v))
         self.mask = None if mask is None else (mask.numpy() != 0).astype(np.uint8)
         self.oracle = oracle
         self.rate = None  # rows per second
+        self.last_rows = None
+        self.last_out = None
 
     def _flops(self, rows):
         w = self.w
@@ -206,29 +210,62 @@ class OracleSampler:
             return float(sum(4.0 * w.D * (i + 1) for i in rows[:, 2]))
         return float(len(rows) * 4.0 * w.D * w.L)
 
+    def _rows(self, g, n):
+        import numpy as np
+        B, H = self.q.shape[0], self.q.shape[1]
+        rows = np.zeros((n, 3), dtype=np.int64)
+        rows[:, 0] = g.integers(0, B, size=n)
+        rows[:, 1] = g.integers(0, H, size=n)
+        rows[:, 2] = g.integers(0, self.w.L, size=n)
+        return rows
+
     def run(self, budget_s: float, seed: int = 0):
         """(algorithmic FLOPs, seconds, rows) for about ``budget_s`` of work."""
         import numpy as np
         g = np.random.default_rng(seed)
         if self.rate is None:
             n0 = max(8, self.oracle.num_threads())
-            rows = np.zeros((n0, 3), dtype=np.int64)
-            rows[:, 2] = g.integers(0, self.w.L, size=n0)
+            rows = self._rows(g, n0)
             t0 = time.perf_counter()
             self.oracle.sdpa_rows(self.q, self.k, self.v, rows, mask=self.mask,
                                   is_causal=self.w.is_causal, scale=self.w.scale)
             self.rate = n0 / max(time.perf_counter() - t0, 1e-6)
         n = max(1, int(self.rate * budget_s))
-        rows = np.zeros((n, 3), dtype=np.int64)
-        rows[:, 2] = g.integers(0, self.w.L, size=n)
+        rows = self._rows(g, n)
         t0 = time.perf_counter()
-        self.oracle.sdpa_rows(self.q, self.k, self.v, rows, mask=self.mask,
-                              is_causal=self.w.is_causal, scale=self.w.scale)
-        return self._flops(rows), time.perf_counter() - t0, n
+        out = self.oracle.sdpa_rows(self.q, self.k, self.v, rows, mask=self.mask,
+                                    is_causal=self.w.is_causal, scale=self.w.scale)
+        dt = time.perf_counter() - t0
+        self.last_rows, self.last_out = rows, out
+        return self._flops(rows), dt, n
 
     @property
     def cores(self):
         return self.oracle.num_threads()
+
+
+PARITY_L2, PARITY_MAX = 1e-2, 2e-2
+
+
+def parity_of(got, ref, rows: int, against: str, extra_ok: bool = True, extra: str = ""):
+    """L2-relative and max-abs error of GPU values ``got`` against oracle
+    values ``ref`` (same shape), and whether both are inside the tolerance
+    (and ``extra_ok``, a further exact check named by ``extra``)."""
+    import numpy as np
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    err = got - ref
+    nref = float(np.linalg.norm(ref))
+    l2 = float(np.linalg.norm(err)) / (nref if nref > 0 else 1.0)
+    mx = float(np.abs(err).max()) if err.size else 0.0
+    finite = bool(np.all(np.isfinite(got)))
+    ok = finite and l2 <= PARITY_L2 and mx <= PARITY_MAX and extra_ok
+    d = {"l2_rel": l2 if finite else None, "max_abs": mx if finite else None, "pass": ok,
+         "rows": rows, "tolerance": {"l2_rel": PARITY_L2, "max_abs": PARITY_MAX},
+         "against": against}
+    if extra:
+        d["exact_check"] = {"what": extra, "pass": bool(extra_ok)}
+    return d
 
 
 # ---------------------------------------------------------------- GPU leg
@@ -324,6 +361,13 @@ def gpu_leg(args, w, rank, world):
         host_us[name] = (time.perf_counter() - t0) / n * 1e6
         stream.synchronize()
 
+    # Inputs that fit in L2 are flushed from it before every timed launch
+    # (a 256 MB write, outside the launch's event pair); larger ones cannot
+    # stay in L2 between steps anyway.
+    flush = None
+    if flush_l2(args, w):
+        flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+
     graph = None
     if args.graph:
         # K plan launches captured once; the timed region replays them with
@@ -353,6 +397,9 @@ def gpu_leg(args, w, rank, world):
     else:
         timed = plan_step if args.plan else step
         for i in range(args.steps):
+            if flush is not None:
+                with torch.cuda.stream(stream):
+                    flush.zero_()   # outside the event pair: L2 holds none of the inputs
             starts[i].record(stream)
             timed()
             ends[i].record(stream)
@@ -366,6 +413,8 @@ def gpu_leg(args, w, rank, world):
         per_launch_ms = [total_ms / args.steps]  # back to back, no host gaps
     else:
         per_launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+        if flush is not None:
+            total_ms = sum(per_launch_ms)  # the K launches, without the flushes between them
     rc, detail = sdpa.sdpa_last_device_status(stream)
     if rc != 0:
         raise RuntimeError(f"timed region reported {sdpa.sdpa_status_string(rc)} ({detail:#x})")
@@ -386,7 +435,8 @@ def gpu_leg(args, w, rank, world):
     d2h = out.numel() * out.element_size()
     plan.close()
     return dict(total_ms=total_ms, per_launch_ms=per_launch_ms, clocks=clk, e2e_ms=e2e_ms,
-                h2d=h2d, d2h=d2h, flops=flops, host_us=host_us)
+                h2d=h2d, d2h=d2h, flops=flops, host_us=host_us, out=out,
+                operands=(q, k, v, mask))
 
 
 def extra_leg(args, path):
@@ -394,10 +444,8 @@ def extra_leg(args, path):
     sparse``): W warm-up launches, then K launches each timed alone with CUDA
     events on the launch stream, the 256 MB L2-flush write between them
     outside the timed pair; e2e through pinned host buffers."""
-    import numpy as np
     import torch
 
-    import oracle
     import scaled_dot_product_forward_gb300 as sdpa
     import sdpa_inputs
 
@@ -485,25 +533,37 @@ def extra_leg(args, path):
                     "h2d_bytes_per_step": sum(x.numel() * x.element_size() for x in ins),
                     "d2h_bytes_per_step": out.numel() * out.element_size(),
                     "ms_per_step": e2e_ms},
-            "gpu_launches": args.steps, "clocks": clk}
+            "gpu_launches": args.steps, "clocks": clk, "parity": None}
     if not args.no_cpu_baseline:
         # the oracle on a bounded sample: one document / a few query rows
+        # the oracle on a bounded sample, whose outputs also check the same
+        # rows of the timed launches' output
+        import oracle
         t0 = time.perf_counter()
         if path == "varlen":
-            n = min(lengths)
-            oracle.sdpa_varlen(q[:n, :1], k[:n, :1], v[:n, :1], [0, n], is_causal=True)
+            d = min(range(len(lengths)), key=lambda i: lengths[i])
+            a, n = int(cu[d]), lengths[d]
+            ref = oracle.sdpa_varlen(q[a:a + n, :1], k[a:a + n, :1], v[a:a + n, :1], [0, n],
+                                     is_causal=True)
+            got = out[a:a + n, :1]
             f = 2.0 * 1 * n * n * D
-            sample = f"one head of one {n}-token document"
+            sample = f"head 0 of the shortest document ({n} tokens)"
+            rows = n
         else:
             rows = 64
             sel = torch.arange(q.shape[0] - rows, q.shape[0])
-            oracle.sdpa_sparse(q[sel], kv, kv, idx[sel].numpy(), topk_length=length[sel].numpy())
+            ref = oracle.sdpa_sparse(q[sel], kv, kv, idx[sel].numpy(),
+                                     topk_length=length[sel].numpy())
+            got = out[sel.to(dev)]
             f = 4.0 * H * D * float(length[sel].sum())
             sample = f"the last {rows} query rows (all heads)"
         t = time.perf_counter() - t0
         line["cpu_baseline"] = {"value": f / t / 1e12, "unit": UNIT,
                                 "cores": oracle.num_threads(), "kind": "oracle",
                                 "sample": f"{sample}, {t:.1f} s"}
+        line["parity"] = parity_of(got.double().cpu().numpy(), ref, rows,
+                                   "fp64 oracle on the cpu_baseline sample of the timed "
+                                   "launches' output")
     return line
 
 
@@ -535,6 +595,11 @@ def main(argv=None):
                     help="time a CUDA graph of K plan launches (no host gaps between kernels)")
     ap.add_argument("--path", choices=["dense", "varlen", "sparse"], default="dense",
                     help="dense (the default contract line), packed documents or sparse top-k")
+    ap.add_argument("--all-workloads", action="store_true",
+                    help="one line per specified dense workload (1-5), each with its roofline "
+                         "and parity")
+    ap.add_argument("--flush-l2", choices=["auto", "yes", "no"], default="auto",
+                    help="auto: flush L2 before each timed launch when the operands fit in it")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -545,51 +610,84 @@ def main(argv=None):
         return 0
 
     import sdpa_inputs
-    w = sdpa_inputs.WORKLOADS[args.workload]
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
-    config = {"workload": w.name, "B": w.B, "H": w.H, "L": w.L, "D": w.D,
-              "launch": ("cuda graph of plan launches" if args.graph else
-                         "sdpa_plan_launch per step" if args.plan else "sdpa_forward per step") +
-                        (" (mask summary kernel + forward)" if (args.graph or args.plan) and
-                         w.p_masked is not None else ""),
-              "is_causal": w.is_causal, "mask": w.p_masked is not None,
-              "rank": w.rank, "scale": "1/sqrt(D)",
-              "l2": "no flush: q, k, v, out total %.0f MB > 129 MB L2" % (
-                  4 * w.heads * w.L * w.D * 2 / 1e6)}
-    dtype = "bf16" if "bf16" in w.name else "fp16"
-
+    wids = sorted(sdpa_inputs.WORKLOADS) if args.all_workloads else [args.workload]
     if args.impl == "reference":
         # The reference arm is the fp64 oracle on the host cores.
         if rank != 0:
             return 0
-        per_step = max(0.02, 120.0 / (args.steps + args.warmup))
-        sampler = OracleSampler(w)
-        for i in range(args.warmup):
-            sampler.run(per_step / 4, seed=1000 + i)
-        tf, tt, rows = 0.0, 0.0, 0
-        for i in range(args.steps):
-            f, t, n = sampler.run(per_step, seed=i + 1)
-            tf, tt, rows = tf + f, tt + t, rows + n
-        cores = sampler.cores
-        val = tf / tt / 1e12
-        line = {"impl": "reference", "metric": METRIC, "value": val, "unit": UNIT,
-                "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-                "ms_per_step": 1e3 * tt / args.steps, "higher_is_better": True,
-                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-                "config": config,
-                "cpu_baseline": {"value": val, "unit": UNIT, "cores": cores, "kind": "oracle",
-                                 "sample": f"{rows} query rows of head (0,0) of the workload, "
-                                           f"{args.steps} steps"},
-                "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0,
-                        "d2h_bytes_per_step": 0}}
-        print(json.dumps(line))
+        for wid in wids:
+            print(json.dumps(reference_line(args, sdpa_inputs.WORKLOADS[wid])), flush=True)
         return 0
 
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group(backend="nccl")
+    for wid in wids:
+        line = dense_line(args, wid, rank, world)
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
 
+
+def flush_l2(args, w) -> bool:
+    """Flush L2 between timed launches: when the operands fit in twice the
+    129 MB L2 (else they cannot stay resident between steps), except under
+    --graph (back-to-back replay) or --flush-l2 no."""
+    if args.graph or args.flush_l2 == "no":
+        return False
+    return args.flush_l2 == "yes" or 4 * w.heads * w.L * w.D * 2 < 2 * 129e6
+
+
+def metric_of(w):
+    return METRIC if w.wid == 3 else f"SDPA fwd TFLOP/s, {w.name}"
+
+
+def config_of(args, w):
+    return {"workload": w.name, "B": w.B, "H": w.H, "L": w.L, "D": w.D,
+            "launch": ("cuda graph of plan launches" if args.graph else
+                       "sdpa_plan_launch per step" if args.plan else "sdpa_forward per step") +
+                      (" (mask summary kernel + forward)" if (args.graph or args.plan) and
+                       w.p_masked is not None else ""),
+            "is_causal": w.is_causal, "mask": w.p_masked is not None,
+            "rank": w.rank, "scale": "1/sqrt(D)",
+            "l2": ("flushed before every timed launch (256 MB write outside the launch's "
+                   "events): q, k, v, out total %.1f MB" if flush_l2(args, w) else
+                   "no flush: q, k, v, out total %.1f MB (> 2 x the 129 MB L2, or a graph "
+                   "replayed back to back)") % (4 * w.heads * w.L * w.D * 2 / 1e6)}
+
+
+def reference_line(args, w):
+    per_step = max(0.02, 120.0 / (args.steps + args.warmup))
+    sampler = OracleSampler(w)
+    for i in range(args.warmup):
+        sampler.run(per_step / 4, seed=1000 + i)
+    tf, tt, rows = 0.0, 0.0, 0
+    for i in range(args.steps):
+        f, t, n = sampler.run(per_step, seed=i + 1)
+        tf, tt, rows = tf + f, tt + t, rows + n
+    cores = sampler.cores
+    val = tf / tt / 1e12
+    return {"impl": "reference", "metric": metric_of(w), "value": val, "unit": UNIT,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * tt / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_of(args, w),
+            "cpu_baseline": {"value": val, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": f"{rows} random query rows (b, h, i) of the workload, "
+                                       f"{args.steps} steps"},
+            "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def dense_line(args, wid, rank, world):
+    import sdpa_inputs
+    w = sdpa_inputs.WORKLOADS[wid]
+    dtype = "bf16" if "bf16" in w.name else "fp16"
     r = gpu_leg(args, w, rank, world)
     total_ms = max_over_ranks(r["total_ms"], world)
     ms_per_step = total_ms / args.steps
@@ -598,12 +696,12 @@ def main(argv=None):
     peak, hbm_peak, peak_kind = load_peaks()
     # A masked plan runs the mask-summary path (its own ncu capture).
     summary = (args.plan or args.graph) and w.p_masked is not None
-    traffic = load_traffic(f"{args.workload}plan" if summary else args.workload)
+    traffic = load_traffic(f"{wid}plan" if summary else wid)
     e2e_ms = max_over_ranks(r["e2e_ms"], world)
-    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": dtype, "data": "synthetic",
-            "config": config,
+    line = {"metric": metric_of(w), "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": dtype,
+            "data": "synthetic", "config": config_of(args, w),
             "roofline": roofline_of(w, r["flops"], mean_launch_ms, peak, hbm_peak, peak_kind,
                                     traffic),
             "e2e": {"value": world * r["flops"] / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
@@ -612,21 +710,33 @@ def main(argv=None):
             "gpu_launches": args.steps * (2 if (args.graph or args.plan) and
                                           w.p_masked is not None else 1),
             "host_us_per_call": r["host_us"],
-            "clocks": r["clocks"]}
+            "clocks": r["clocks"], "parity": None}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        sampler = OracleSampler(w)
+        # The oracle leg: timed on random rows of the workload, whose outputs
+        # then check the same rows of the timed launches' output.
+        sampler = OracleSampler(w, r["operands"])
         f, t, rows = sampler.run(args.cpu_budget_s)
         cores = sampler.cores
         line["cpu_baseline"] = {"value": f / t / 1e12, "unit": UNIT, "cores": cores,
                                 "kind": "oracle",
-                                "sample": f"{rows} random query rows of head (0,0), "
+                                "sample": f"{rows} random query rows (b, h, i) of the workload, "
                                           f"algorithmic FLOPs of those rows, {t:.1f} s"}
-    if rank == 0:
-        print(json.dumps(line))
-    if world > 1:
-        import torch.distributed as dist
-        dist.destroy_process_group()
-    return 0
+        out = r["out"]
+        got_all = out if w.rank == 4 else out[None]
+        idx = sampler.last_rows
+        import torch
+        ti = torch.as_tensor(idx, device=out.device)
+        got = got_all[ti[:, 0], ti[:, 1], ti[:, 2]].double().cpu().numpy()
+        extra_ok, extra = True, ""
+        if w.p_masked is not None:
+            dead = sdpa_inputs.full_rows(w).to(out.device)
+            extra_ok = bool(torch.all(got_all[:, :, dead, :] == 0).item())
+            extra = f"all {len(dead)} fully masked rows of every head exactly zero"
+        line["parity"] = parity_of(got, sampler.last_out, rows,
+                                   "fp64 oracle on the cpu_baseline sample's rows of the "
+                                   "timed launches' output", extra_ok, extra)
+    del r
+    return line
 
 
 if __name__ == "__main__":

@@ -176,7 +176,10 @@ SDPA_API void sdpa_plan_destroy(sdpa_plan* plan);
  * The caller passes and owns q, k, v, out and mask; the call allocates no
  * device or pinned memory.  The first call on a device looks up the array's
  * device address on that device (it must be current, as for every call) and
- * caches it; make that first call before any stream capture.  Every call
+ * caches it; make that first call before any stream capture.  The cached
+ * address belongs to the device's context: after cudaDeviceReset the next
+ * call finds that the context changed and looks the address up again (so
+ * that call, too, belongs before any capture).  Every call
  * on a device uses the same array and leaves its last summary in it:
  * nothing there needs to start at zero, because each call rewrites every
  * byte it then reads, but calls whose work overlaps on the GPU (different
@@ -344,9 +347,14 @@ SDPA_API const char* sdpa_status_string(sdpa_status status);
  * the kernel is bounded in time; on expiry the kernel stops, frees its
  * resources and sets a device status word instead of hanging).  Returns
  * SDPA_OK, SDPA_ERR_DEVICE_TIMEOUT (the word is then cleared), or
- * SDPA_ERR_CUDA.  When `detail` is not NULL it receives the raw status bits.
+ * SDPA_ERR_CUDA.
+ *
+ * sdpa_last_device_status_detail -- the same query; when `detail` is not
+ * NULL it also receives the raw status bits (bit 0: a wait ran out of time;
+ * the higher bits name the kind of wait), for diagnostics.
  */
-SDPA_API sdpa_status sdpa_last_device_status(void* stream, uint32_t* detail);
+SDPA_API sdpa_status sdpa_last_device_status(void* stream);
+SDPA_API sdpa_status sdpa_last_device_status_detail(void* stream, uint32_t* detail);
 
 /* ABI version: major * 10000 + minor * 100 + patch. */
 SDPA_API int sdpa_version(void);

@@ -21,7 +21,7 @@ __all__ = ["sdpa_forward", "sdpa_forward_raw", "sdpa_status_string", "sdpa_last_
            "sdpa_version", "SdpaError", "load_library", "LIB_PATH", "STATUS",
            "sdpa_debug_set_wait_limit_ns", "sdpa_debug_withhold_q_load", "sdpa_debug_exp2_poly",
            "sdpa_forward_varlen", "sdpa_sparse_forward", "sdpa_sparse_compact", "SdpaPlan",
-           "sdpa_mask_tiles"]
+           "sdpa_mask_tiles", "sdpa_forward_masked_noalloc"]
 
 LIB_PATH = _build.LIB_PATH
 
@@ -59,8 +59,10 @@ def load_library(path: str | None = None):
     lib.sdpa_forward.restype = ctypes.c_int
     lib.sdpa_status_string.argtypes = [ctypes.c_int]
     lib.sdpa_status_string.restype = ctypes.c_char_p
-    lib.sdpa_last_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
+    lib.sdpa_last_device_status.argtypes = [vp]
     lib.sdpa_last_device_status.restype = ctypes.c_int
+    lib.sdpa_last_device_status_detail.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
+    lib.sdpa_last_device_status_detail.restype = ctypes.c_int
     lib.sdpa_version.argtypes = []
     lib.sdpa_version.restype = ctypes.c_int
     lib.sdpa_debug_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
@@ -101,6 +103,9 @@ def load_library(path: str | None = None):
     lib.sdpa_sparse_compact.restype = ctypes.c_int
     lib.sdpa_mask_tiles.argtypes = [vp, ctypes.c_int64, vp, vp, vp]
     lib.sdpa_mask_tiles.restype = ctypes.c_int
+    lib.sdpa_forward_masked_noalloc.argtypes = [vp, vp, vp, vp, ctypes.c_int, ctypes.c_int, i64p,
+                                                i64p, i64p, i64p, i64p, vp, ctypes.c_float, vp]
+    lib.sdpa_forward_masked_noalloc.restype = ctypes.c_int
     if path is None:
         _lib = lib
     return lib
@@ -212,6 +217,26 @@ def sdpa_forward(q, k, v, out=None, *, is_causal: bool = False, mask=None, scale
     if rc != 0:
         raise SdpaError(rc, "sdpa_forward_lse")
     return out, lse
+
+
+def sdpa_forward_masked_noalloc(q, k, v, mask, out, *, scale=None, stream=None) -> int:
+    """Masked forward whose mask summary lives in the library's fixed device
+    array (sdpa_forward_masked_noalloc): nothing is allocated, so ``out``
+    must be passed.  Returns the status code without raising (the caller
+    decides; SDPA_ERR_SHAPE = 3 for L beyond the array's limit)."""
+    import torch
+
+    if q.dtype not in (torch.bfloat16, torch.float16):
+        return 4
+    mp = _mask_ptr(mask)
+    s = float("nan") if scale is None else float(scale)
+    st = (stream if stream is not None else torch.cuda.current_stream(q.device)).cuda_stream
+    return int(load_library().sdpa_forward_masked_noalloc(
+        ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k.data_ptr()),
+        ctypes.c_void_p(v.data_ptr()), ctypes.c_void_p(out.data_ptr()), _dtype_code(q), q.dim(),
+        _arr(q.shape), _arr(q.stride()), _arr(k.stride()), _arr(v.stride()), _arr(out.stride()),
+        ctypes.c_void_p(mp) if mp else None, ctypes.c_float(s),
+        ctypes.c_void_p(st) if st else None))
 
 
 def sdpa_forward_varlen(q, k, v, cu_seqlens, max_seqlen, out=None, *, is_causal: bool = False,
@@ -443,13 +468,15 @@ class SdpaPlan:
 
 
 def sdpa_last_device_status(stream=None):
-    """(status, detail bits) after synchronising ``stream``."""
+    """(status, detail bits) after synchronising ``stream``
+    (sdpa_last_device_status_detail; sdpa_last_device_status is the same
+    query without the bits)."""
     import torch
 
     st = (stream if stream is not None else torch.cuda.current_stream()).cuda_stream
     detail = ctypes.c_uint32(0)
-    rc = load_library().sdpa_last_device_status(ctypes.c_void_p(st) if st else None,
-                                                ctypes.byref(detail))
+    rc = load_library().sdpa_last_device_status_detail(ctypes.c_void_p(st) if st else None,
+                                                       ctypes.byref(detail))
     return int(rc), int(detail.value)
 
 

@@ -805,7 +805,7 @@ const char* sdpa_status_string(sdpa_status status) {
   return "SDPA_UNKNOWN_STATUS";
 }
 
-sdpa_status sdpa_last_device_status(void* stream, uint32_t* detail) {
+sdpa_status sdpa_last_device_status_detail(void* stream, uint32_t* detail) {
   unsigned int st = 0, st_sparse = 0;
   if (sdpa_impl::read_and_clear_device_status(static_cast<cudaStream_t>(stream), &st) !=
           cudaSuccess ||
@@ -814,6 +814,10 @@ sdpa_status sdpa_last_device_status(void* stream, uint32_t* detail) {
   st |= st_sparse;
   if (detail) *detail = st;
   return st == 0 ? SDPA_OK : SDPA_ERR_DEVICE_TIMEOUT;
+}
+
+sdpa_status sdpa_last_device_status(void* stream) {
+  return sdpa_last_device_status_detail(stream, nullptr);
 }
 
 int sdpa_version(void) { return 100; }

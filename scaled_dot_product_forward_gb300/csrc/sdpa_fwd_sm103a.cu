@@ -1401,20 +1401,60 @@ cudaError_t launch_forward(const FwdParams& p, int head_dim, int mask_mode, bool
 cudaError_t noalloc_mask_tiles(int device, const uint4** tile_bits,
                                const uint8_t** tile_class) {
   // One cached device address per device, found the first time a device
-  // asks (with that device current, as cudaGetSymbolAddress requires).
+  // asks (with that device current, as cudaGetSymbolAddress requires) and
+  // found again whenever the device's current context is a different one:
+  // after cudaDeviceReset the runtime creates a new primary context and
+  // loads the module again, and the old address no longer maps anything.
+  // Contexts are told apart by their process-unique ids (cuCtxGetId).
+  using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+  using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+  static std::once_flag once;
+  static CtxGetCurrentFn ctx_current = nullptr;
+  static CtxGetIdFn ctx_id = nullptr;
+  std::call_once(once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      ctx_current = reinterpret_cast<CtxGetCurrentFn>(fn);
+    fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      ctx_id = reinterpret_cast<CtxGetIdFn>(fn);
+  });
   static std::mutex mu;
   static void* addr[kNoAllocMaxDevices] = {};
+  static unsigned long long addr_ctx[kNoAllocMaxDevices] = {};
   if (device < 0 || device >= kNoAllocMaxDevices) return cudaErrorInvalidDevice;
+  if (ctx_current == nullptr || ctx_id == nullptr) return cudaErrorNotSupported;
+  int cur = -1;
+  cudaError_t e = cudaGetDevice(&cur);
+  if (e != cudaSuccess) return e;
+  if (cur != device) return cudaErrorInvalidDevice;
+  // The id of the context the runtime has made current for this device; 0
+  // when there is none yet (no runtime call has needed it so far) or the
+  // handle left current no longer names a live context.
+  auto current_id = [&]() -> unsigned long long {
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (ctx_current(&ctx) != CUDA_SUCCESS || ctx == nullptr || ctx_id(ctx, &id) != CUDA_SUCCESS)
+      return 0;
+    return id;
+  };
+  unsigned long long id = current_id();
   std::lock_guard<std::mutex> lock(mu);
-  if (addr[device] == nullptr) {
-    int cur = -1;
-    cudaError_t e = cudaGetDevice(&cur);
-    if (e != cudaSuccess) return e;
-    if (cur != device) return cudaErrorInvalidDevice;
+  if (addr[device] == nullptr || id == 0 || addr_ctx[device] != id) {
+    // cudaGetSymbolAddress also makes the device's primary context current
+    // (creating it after a reset), so the id is read again afterwards.
     void* ptr = nullptr;
     e = cudaGetSymbolAddress(&ptr, g_noalloc_mask_tiles);
     if (e != cudaSuccess) return e;
+    id = current_id();
+    if (id == 0) return cudaErrorDeviceUninitialized;
     addr[device] = ptr;
+    addr_ctx[device] = id;
   }
   *tile_bits = static_cast<const uint4*>(addr[device]);
   *tile_class = static_cast<const uint8_t*>(addr[device]) +

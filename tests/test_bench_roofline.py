@@ -35,3 +35,42 @@ def test_source_hash_ignores_comments_but_not_code():
     c = "int f() {\n  return 2;\n}\n"
     assert bench.code_of(a) == bench.code_of(b)
     assert bench.code_of(a) != bench.code_of(c)
+
+
+def test_parity_block_passes_and_fails_on_the_tolerance():
+    import numpy as np
+    ref = np.linspace(-1.0, 1.0, 64).reshape(4, 16)
+    ok = bench.parity_of(ref + 1e-4, ref, 4, "test")
+    assert ok["pass"] and ok["rows"] == 4 and ok["max_abs"] < 2e-4
+    bad = ref.copy()
+    bad[2, 3] += 0.05                                   # one element past max-abs 2e-2
+    assert not bench.parity_of(bad, ref, 4, "test")["pass"]
+    nan = ref.copy()
+    nan[0, 0] = np.nan
+    assert not bench.parity_of(nan, ref, 4, "test")["pass"]
+    assert not bench.parity_of(ref, ref, 4, "test", extra_ok=False, extra="dead rows")["pass"]
+
+
+def test_oracle_sampler_rows_are_the_oracles_rows():
+    """The CPU leg's sample (random (b, h, i) rows over every head) and the
+    outputs it keeps for the parity check are the oracle's own rows."""
+    import numpy as np
+    import oracle
+    w = sdpa_inputs.WORKLOADS[1]
+    s = bench.OracleSampler(w)
+    _, _, n = s.run(0.05, seed=3)
+    assert s.last_rows.shape == (n, 3) and s.last_out.shape == (n, w.D)
+    q, k, v, _ = sdpa_inputs.make(w)
+    full = oracle.sdpa(q, k, v, is_causal=True)
+    r = s.last_rows
+    assert np.array_equal(full[r[:, 1], r[:, 2]], s.last_out)
+    assert set(r[:, 1]) <= set(range(w.H)) and np.all(r[:, 0] == 0)
+
+
+def test_l2_flush_follows_operand_size():
+    import argparse
+    a = argparse.Namespace(graph=False, flush_l2="auto")
+    ws = sdpa_inputs.WORKLOADS
+    assert [bench.flush_l2(a, ws[i]) for i in (1, 2, 3, 4, 5)] == [True, True, False, True, False]
+    a.graph = True
+    assert not bench.flush_l2(a, ws[2])
