@@ -371,16 +371,6 @@ SDPA_API int sdpa_version(void);
 SDPA_API void sdpa_debug_set_wait_limit_ns(uint64_t ns);
 SDPA_API void sdpa_debug_withhold_q_load(int enable);
 
-/*
- * Test hook: y[i] = 2^x[i] for n DEVICE floats, evaluated with the kernel's
- * FMA-pipe exponential (range reduction plus a minimax cubic; relative error
- * about 1e-4, inputs at or below -127 give exactly 0).  The kernel computes
- * part of the softmax probabilities this way; this entry point exists so the
- * tests can bound its error against the exact exponential.  Asynchronous on
- * `stream`; returns SDPA_ERR_NULL / SDPA_ERR_SHAPE / SDPA_ERR_CUDA on error.
- */
-SDPA_API sdpa_status sdpa_debug_exp2_poly(const float* x, float* y, int64_t n, void* stream);
-
 #ifdef __cplusplus
 }
 #endif

@@ -19,7 +19,7 @@ from . import _build
 
 __all__ = ["sdpa_forward", "sdpa_forward_raw", "sdpa_status_string", "sdpa_last_device_status",
            "sdpa_version", "SdpaError", "load_library", "LIB_PATH", "STATUS",
-           "sdpa_debug_set_wait_limit_ns", "sdpa_debug_withhold_q_load", "sdpa_debug_exp2_poly",
+           "sdpa_debug_set_wait_limit_ns", "sdpa_debug_withhold_q_load",
            "sdpa_forward_varlen", "sdpa_sparse_forward", "sdpa_sparse_compact", "SdpaPlan",
            "sdpa_mask_tiles", "sdpa_forward_masked_noalloc"]
 
@@ -69,8 +69,6 @@ def load_library(path: str | None = None):
     lib.sdpa_debug_set_wait_limit_ns.restype = None
     lib.sdpa_debug_withhold_q_load.argtypes = [ctypes.c_int]
     lib.sdpa_debug_withhold_q_load.restype = None
-    lib.sdpa_debug_exp2_poly.argtypes = [vp, vp, ctypes.c_int64, vp]
-    lib.sdpa_debug_exp2_poly.restype = ctypes.c_int
     lib.sdpa_plan_create.argtypes = [ctypes.POINTER(vp), vp, vp, vp, vp, ctypes.c_int,
                                      ctypes.c_int, i64p, i64p, i64p, i64p, i64p, ctypes.c_int,
                                      vp, ctypes.c_float]
@@ -125,20 +123,6 @@ def sdpa_debug_set_wait_limit_ns(ns: int) -> None:
 
 def sdpa_debug_withhold_q_load(enable: bool) -> None:
     load_library().sdpa_debug_withhold_q_load(1 if enable else 0)
-
-
-def sdpa_debug_exp2_poly(x):
-    """2^x (float32 CUDA tensor) through the kernel's FMA-pipe polynomial."""
-    import torch
-    x = x.contiguous()
-    y = torch.empty_like(x)
-    st = torch.cuda.current_stream(x.device).cuda_stream
-    rc = load_library().sdpa_debug_exp2_poly(ctypes.c_void_p(x.data_ptr()),
-                                             ctypes.c_void_p(y.data_ptr()), x.numel(),
-                                             ctypes.c_void_p(st) if st else None)
-    if rc != 0:
-        raise SdpaError(rc, "sdpa_debug_exp2_poly")
-    return y
 
 
 def _arr(vals):

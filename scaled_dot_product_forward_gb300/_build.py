@@ -17,7 +17,7 @@ INCLUDE = os.path.join(os.path.dirname(PKG), "include")
 LIB_NAME = "libsdpa_gb300.so"
 LIB_PATH = os.path.join(PKG, LIB_NAME)
 
-SOURCES = ["sdpa_fwd_sm103a.cu", "sdpa_sparse_sm103a.cu", "sdpa_api.cpp"]
+SOURCES = ["sdpa_fwd_sm103a.cu", "sdpa_fwd64_sm103a.cu", "sdpa_sparse_sm103a.cu", "sdpa_api.cpp"]
 GENCODE = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
           "-Xcompiler", "-fvisibility=hidden", "-I", INCLUDE, "-I", CSRC]

@@ -252,6 +252,72 @@ __device__ __forceinline__ void mma_ts_elect(uint32_t d_tmem, uint32_t a_tmem, u
       "r"(a_tmem), "r"(b_lo), "r"(idesc), "r"(accumulate), "n"(B_HI)
       : "memory");
 }
+// Four consecutive K-steps in one elected issue: D[tmem] (+)= A[smem] *
+// B[smem]^T with the descriptors' low words advancing by a_step / b_step
+// (16-byte units) per step; the first step accumulates when acc != 0, the
+// others always.
+template <uint32_t A_HI, uint32_t B_HI>
+__device__ __forceinline__ void mma_ss_x4(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo,
+                                          uint32_t a_step, uint32_t b_step, uint32_t idesc,
+                                          uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p, e, q;\n\t.reg .b32 a, b;\n\t.reg .b64 da, db;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "setp.eq.b32 q, %4, %4;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "mov.b64 da, {%1, %7};\n\t"
+      "mov.b64 db, {%2, %8};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, p;\n\t"
+      "add.u32 a, %1, %5;\n\t"
+      "add.u32 b, %2, %6;\n\t"
+      "mov.b64 da, {a, %7};\n\t"
+      "mov.b64 db, {b, %8};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, q;\n\t"
+      "add.u32 a, a, %5;\n\t"
+      "add.u32 b, b, %6;\n\t"
+      "mov.b64 da, {a, %7};\n\t"
+      "mov.b64 db, {b, %8};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, q;\n\t"
+      "add.u32 a, a, %5;\n\t"
+      "add.u32 b, b, %6;\n\t"
+      "mov.b64 da, {a, %7};\n\t"
+      "mov.b64 db, {b, %8};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, q;\n\t}" ::"r"(d_tmem),
+      "r"(a_lo), "r"(b_lo), "r"(idesc), "r"(acc), "r"(a_step), "r"(b_step), "n"(A_HI),
+      "n"(B_HI)
+      : "memory");
+}
+
+// Four consecutive K-steps in one elected issue: D[tmem] (+)= A[tmem] *
+// B[smem], the TMEM column of A advancing by a_step and B's descriptor low
+// word by b_step per step.
+template <uint32_t B_HI>
+__device__ __forceinline__ void mma_ts_x4(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo,
+                                          uint32_t a_step, uint32_t b_step, uint32_t idesc,
+                                          uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p, e, q;\n\t.reg .b32 a, b;\n\t.reg .b64 db;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "setp.eq.b32 q, %4, %4;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "mov.b64 db, {%2, %7};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %3, p;\n\t"
+      "add.u32 a, %1, %5;\n\t"
+      "add.u32 b, %2, %6;\n\t"
+      "mov.b64 db, {b, %7};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], db, %3, q;\n\t"
+      "add.u32 a, a, %5;\n\t"
+      "add.u32 b, b, %6;\n\t"
+      "mov.b64 db, {b, %7};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], db, %3, q;\n\t"
+      "add.u32 a, a, %5;\n\t"
+      "add.u32 b, b, %6;\n\t"
+      "mov.b64 db, {b, %7};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], db, %3, q;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(b_lo), "r"(idesc), "r"(acc), "r"(a_step), "r"(b_step), "n"(B_HI)
+      : "memory");
+}
+
 __device__ __forceinline__ void mma_commit_elect(uint64_t* bar) {
   asm volatile(
       "{\n\t.reg .pred e;\n\t"
@@ -321,6 +387,17 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
       : "memory");
 }
 
+// 32 lanes x 16 consecutive 32-bit columns (the half-width store).
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15])
+      : "memory");
+}
+
 __device__ __forceinline__ void tmem_ld_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
@@ -361,17 +438,6 @@ __device__ __forceinline__ void fma2_bcast(float& o0, float& o1, float a0, float
       : "=f"(o0), "=f"(o1)
       : "f"(a0), "f"(a1), "f"(b), "f"(c));
 }
-// (q0, q1) = (q0, q1) * (f0, f1) + c (c broadcast)
-__device__ __forceinline__ void fma2_mul_add(float& q0, float& q1, float f0, float f1, float c) {
-  asm("{\n\t.reg .b64 rq, rf, rc;\n\t"
-      "mov.b64 rq, {%0, %1};\n\t"
-      "mov.b64 rf, {%2, %3};\n\t"
-      "mov.b64 rc, {%4, %4};\n\t"
-      "fma.rn.f32x2 rq, rq, rf, rc;\n\t"
-      "mov.b64 {%0, %1}, rq;\n\t}"
-      : "+f"(q0), "+f"(q1)
-      : "f"(f0), "f"(f1), "f"(c));
-}
 // (a0, a1) += (b0, b1)
 __device__ __forceinline__ void add2_acc(float& a0, float& a1, float b0, float b1) {
   asm("{\n\t.reg .b64 ra, rb;\n\t"
@@ -392,38 +458,6 @@ __device__ __forceinline__ void mul2_bcast(float& a0, float& a1, float b) {
       : "+f"(a0), "+f"(a1)
       : "f"(b));
 }
-// Base-2 exponential of two values on the FMA/ALU pipes instead of MUFU
-// (Cody-Waite range reduction plus a minimax cubic).  2^x = 2^n * 2^f with
-// n = round(x) taken by adding 1.5 * 2^23 (the sum's low mantissa bits hold
-// n), f = x - n in [-1/2, 1/2], and 2^f ~ 1 + f (c1 + f (c2 + f c3)); 2^n is
-// applied by adding n to the exponent field.  Inputs below -127 are clamped
-// to -127, which returns exactly +0.0 (c0 = 1 exactly), so removed scores
-// (-inf) still give probability 0.  Maximum relative error 1.02e-4 on the
-// whole range; c1..c3 come from scaled_dot_product_forward_gb300/
-// fit_exp2_poly.py (a minimax fit solved as a linear program).
-constexpr float kExp2C1 = 6.932829022e-01f;  // 0x3f317afd
-constexpr float kExp2C2 = 2.422109693e-01f;  // 0x3e780627
-constexpr float kExp2C3 = 5.500905961e-02f;  // 0x3d61512e
-
-__device__ __forceinline__ void ex2_poly2(float& y0, float& y1, float x0, float x1) {
-  constexpr float kRound = 12582912.0f;  // 1.5 * 2^23
-  x0 = fmaxf(x0, -127.0f);
-  x1 = fmaxf(x1, -127.0f);
-  float t0 = x0, t1 = x1;
-  add2_acc(t0, t1, kRound, kRound);  // t = x + 1.5*2^23: rounds x to an integer
-  float n0 = t0, n1 = t1;
-  add2_acc(n0, n1, -kRound, -kRound);  // n = round(x) as a float
-  float f0 = -n0, f1 = -n1;
-  add2_acc(f0, f1, x0, x1);  // f = x - n
-  float q0, q1;
-  fma2_bcast(q0, q1, f0, f1, kExp2C3, kExp2C2);  // c3 f + c2
-  fma2_mul_add(q0, q1, f0, f1, kExp2C1);        // (.) f + c1
-  fma2_mul_add(q0, q1, f0, f1, 1.0f);           // (.) f + 1
-  // add n (the low bits of t) to the exponent field
-  y0 = __int_as_float(__float_as_int(t0) * (1 << 23) + __float_as_int(q0));
-  y1 = __int_as_float(__float_as_int(t1) * (1 << 23) + __float_as_int(q1));
-}
-
 // Three-input maximum / minimum.
 __device__ __forceinline__ float max3f(float a, float b, float c) {
   float d;

@@ -806,12 +806,13 @@ const char* sdpa_status_string(sdpa_status status) {
 }
 
 sdpa_status sdpa_last_device_status_detail(void* stream, uint32_t* detail) {
-  unsigned int st = 0, st_sparse = 0;
+  unsigned int st = 0, st64 = 0, st_sparse = 0;
   if (sdpa_impl::read_and_clear_device_status(static_cast<cudaStream_t>(stream), &st) !=
           cudaSuccess ||
+      sdpa_impl::read_and_clear_fwd64_status(&st64) != cudaSuccess ||
       sdpa_impl::read_and_clear_sparse_status(&st_sparse) != cudaSuccess)
     return SDPA_ERR_CUDA;
-  st |= st_sparse;
+  st |= st64 | st_sparse;
   if (detail) *detail = st;
   return st == 0 ? SDPA_OK : SDPA_ERR_DEVICE_TIMEOUT;
 }
@@ -824,16 +825,6 @@ int sdpa_version(void) { return 100; }
 
 void sdpa_debug_set_wait_limit_ns(uint64_t ns) {
   g_wait_limit_ns.store(ns == 0 ? kDefaultWaitLimitNs : ns, std::memory_order_relaxed);
-}
-
-sdpa_status sdpa_debug_exp2_poly(const float* x, float* y, int64_t n, void* stream) {
-  if (!x || !y) return SDPA_ERR_NULL;
-  if (n < 0 || n > (int64_t(1) << 31)) return SDPA_ERR_SHAPE;
-  const sdpa_status s = check_device();
-  if (s != SDPA_OK) return s;
-  return sdpa_impl::launch_exp2_poly(x, y, n, static_cast<cudaStream_t>(stream)) == cudaSuccess
-             ? SDPA_OK
-             : SDPA_ERR_CUDA;
 }
 
 void sdpa_debug_withhold_q_load(int enable) {

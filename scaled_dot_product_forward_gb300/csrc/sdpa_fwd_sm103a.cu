@@ -1,4 +1,5 @@
-// sdpa_fwd_sm103a.cu -- fused scaled dot-product attention forward for sm_103a.
+// sdpa_fwd_sm103a.cu -- fused scaled dot-product attention forward for sm_103a,
+// head size 128 (head size 64 has its own kernel in sdpa_fwd64_sm103a.cu).
 //
 // Computes, per (batch, head), out = softmax(scale * Q K^T with causal or
 // boolean masking) V: the five-step attention of "Profiling attention in
@@ -9,25 +10,19 @@
 // HBM -- but built for Blackwell:
 //
 //   * persistent: at most one CTA per SM, each walking a static share of
-//     the work.  A job is a pair of adjacent 128-row query tiles (A = rows
-//     256m.., B = rows 256m+128..) of one (batch, head); a unit is the causal
-//     pair P-1-k followed by pair k of the same head, so every unit costs the
-//     same number of key tiles.  Units are head-major, so the CTAs busy at
-//     one time share a few heads' K/V in L2.  Problems whose K and V fit in
-//     L2 deal jobs by falling cost in snake order over the CTAs instead;
-//     packed documents are found through a warp-wide cursor over cu_seqlens
-//     (and, with at most 32 of them, dealt by cost as well).  The next job's
-//     Q load and first S products overlap the previous job's epilogue;
+//     the work (sdpa_sched.cuh).  A job is a pair of adjacent 128-row query
+//     tiles (A = rows 256m.., B = rows 256m+128..) of one (batch, head); a
+//     unit is the causal pair P-1-k followed by pair k of the same head, so
+//     every unit costs the same number of key tiles.  The next job's Q load
+//     and first S products overlap the previous job's epilogue;
 //   * warp 0 streams each job's Q_A, Q_B and one ring of K and V tiles that
 //     runs on across jobs, with TMA (128-byte swizzled boxes of 64 x 128
 //     elements), K and V with their own full/empty barriers;
-//   * warp 1 issues tcgen05.mma (one elected lane).  D = 128, in the order
+//   * warp 1 issues tcgen05.mma (one elected lane) in the order
 //       S_A(0) S_B(0) | PV_A(0) S_A(1) PV_B(0) S_B(1) | PV_A(1) S_A(2) ...
 //     so that while one softmax warpgroup works on its tile the tensor core
 //     is busy with the other tile's products; S = Q K^T lands in TMEM, and
-//     P (16-bit, written over S) is read from TMEM by O += P V.  D = 64 has
-//     room for P beside S, so S(j+1) of both tiles is issued as soon as the
-//     softmax has loaded S(j), ahead of PV(j);
+//     P (16-bit, written over S) is read from TMEM by O += P V;
 //   * warpgroup 1 owns tile A, warpgroup 2 tile B: one query row per thread
 //     (TMEM lane = row), so row max and row sum are in-thread tree
 //     reductions with no shuffles; scale, causal / explicit / ragged-tail
@@ -51,8 +46,10 @@
 
 #include "ptx.cuh"
 #include "sdpa_internal.h"
+#include "sdpa_sched.cuh"
 
 using namespace sdpa_dev;
+using namespace sdpa_sched;
 
 // Device status word: bit 0 = some barrier wait ran out of time; the upper
 // bits name the wait site.  Read and cleared by sdpa_last_device_status().
@@ -70,8 +67,6 @@ static __device__ __align__(256) uint8_t
 
 namespace {
 
-constexpr int kBlockM = 128;   // query rows per tile (TMEM lanes)
-constexpr int kBlockN = 128;   // keys per tile
 constexpr int kTilesPerCta = 2;
 constexpr int kThreads = 384;  // WG0: TMA warp, MMA warp, 2 spare; WG1: tile A; WG2: tile B
 // Register split: the launch reserves kLaunchRegs per thread (the cap that
@@ -84,33 +79,12 @@ constexpr uint32_t kRegsSoftmax = 208;
 static_assert(128 * kRegsControl + 256 * kRegsSoftmax <= kThreads * kLaunchRegs,
               "register split exceeds the launch allocation");
 constexpr float kRescaleLog2 = 8.0f;  // rescale O only when max grows by > 2^8
+constexpr int D = 128;
 
-// With D = 64 the two output accumulators take only 128 TMEM columns, which
-// leaves room for P in its own 64-column buffers.  Then S(j+1) no longer has
-// to wait for PV(j) to consume P(j): it is issued as soon as the softmax has
-// loaded S(j) into registers, and each softmax warpgroup runs tile after
-// tile without waiting for its own products.  With D = 128 the 512 columns
-// are all used (S_A, S_B, O_A, O_B) and P is written over S.
-template <int D>
-struct TmemPlan {
-  static constexpr bool kEarlyS = (D == 64);
-  __host__ __device__ static constexpr uint32_t s_col(int t) { return t ? 128u : 0u; }
-  __host__ __device__ static constexpr uint32_t o_col(int t) { return t ? 256u + D : 256u; }
-  __host__ __device__ static constexpr uint32_t p_col(int t) {
-    return kEarlyS ? (t ? 256u + 2 * D + 64 : 256u + 2 * D) : s_col(t);
-  }
-  static_assert(!kEarlyS || 256 + 2 * D + 128 <= 512, "TMEM plan exceeds 512 columns");
-};
-
-// When nonzero, one pair of exponentials in every kPolyPeriod goes through
-// the FMA-pipe polynomial instead of MUFU.  Off: on GB300 the exponential
-// unit is not the binding limit of this loop (offloading a quarter of the
-// pairs lowered the [4,32,4096,128] causal rate from 1235 to 1177 TFLOP/s,
-// the extra instructions costing more issue slots than MUFU time saved).
-constexpr int kPolyPeriod = 0;
-__host__ __device__ constexpr bool poly_pair(int pair) {
-  return kPolyPeriod > 0 && pair % (kPolyPeriod > 0 ? kPolyPeriod : 1) == kPolyPeriod - 1;
-}
+// TMEM (512 columns): S_A [0,128), S_B [128,256), O_A [256,384), O_B
+// [384,512); P_t (16-bit pairs) is written over the first 64 columns of S_t.
+__host__ __device__ constexpr uint32_t s_col(int t) { return t ? 128u : 0u; }
+__host__ __device__ constexpr uint32_t o_col(int t) { return t ? 256u + D : 256u; }
 constexpr uint32_t kTmemCols = 512;
 
 enum WaitSite : unsigned int {
@@ -122,21 +96,18 @@ enum WaitSite : unsigned int {
   kSiteODone = 1u << 6,
   kSiteDrain = 1u << 7,
   kSiteVFull = 1u << 8,
-  kSiteSFree = 1u << 9,
 };
 
-template <int D>
 struct Layout {
   static constexpr int kChunks = D / 64;               // 128-byte swizzle atoms along D
   static constexpr int kChunkBytes = kBlockM * 128;    // one 128-row x 64-element box
   static constexpr int kTileBytes = kChunks * kChunkBytes;
-  // Ring depths.  With D = 128 there is room for five 32 KB tiles beside Q
-  // (64 KB).  A stage of K is refilled once S of both tiles has read it and
-  // that tile is needed again 2.5 products-pairs later, earlier than V
-  // (refilled after PV of both tiles, needed three pairs later), so K gets
-  // the third stage.
-  static constexpr int kKStages = (D == 64) ? 6 : 3;
-  static constexpr int kVStages = (D == 64) ? 6 : 2;
+  // Ring depths: five 32 KB tiles fit beside Q (64 KB).  A stage of K is
+  // refilled once S of both tiles has read it and that tile is needed again
+  // 2.5 product pairs later, earlier than V (refilled after PV of both
+  // tiles, needed three pairs later), so K gets the third stage.
+  static constexpr int kKStages = 3;
+  static constexpr int kVStages = 2;
   static constexpr int kQ = 0;
   static constexpr int kK = kQ + kTilesPerCta * kTileBytes;
   static constexpr int kV = kK + kKStages * kTileBytes;
@@ -152,7 +123,6 @@ struct Barriers {
   uint64_t s_full[kTilesPerCta];
   uint64_t p_ready[kTilesPerCta];
   uint64_t o_done[kTilesPerCta];
-  uint64_t s_free[kTilesPerCta];  // S(j) loaded by the softmax (early-S plan only)
   uint64_t o_free[kTilesPerCta];  // the job's O_t read by its epilogue
   uint64_t fin;
   uint64_t k_full[kMaxStages];
@@ -162,35 +132,17 @@ struct Barriers {
   uint32_t tmem_base;
   uint32_t abort_flag;
 };
-static_assert(sizeof(Barriers) <= 512, "barrier block too large");
-static_assert(Layout<128>::kTotal <= 227 * 1024, "shared memory over the per-CTA limit");
-static_assert(Layout<64>::kTotal <= 227 * 1024, "shared memory over the per-CTA limit");
-static_assert(Layout<64>::kKStages <= kMaxStages && Layout<128>::kKStages <= kMaxStages &&
-                  Layout<64>::kVStages <= kMaxStages && Layout<128>::kVStages <= kMaxStages,
-              "ring");
+static_assert(sizeof(Barriers) <= Layout::kBarBytes, "barrier block too large");
+static_assert(Layout::kTotal <= 227 * 1024, "shared memory over the per-CTA limit");
+static_assert(Layout::kKStages <= kMaxStages && Layout::kVStages <= kMaxStages, "ring");
 
-// Bounded wait on one barrier phase.  Returns false when the wait gave up:
-// either another role already raised the CTA abort flag (honour_abort), or
-// this wait exceeded the time limit, in which case it raises the flag and
-// records `site` in the device status word.
+// Bounded wait on one barrier phase (sdpa_sched::wait_phase with this CTA's
+// abort flag and this kernel's status word).
 __device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, Barriers* bars,
                                            uint64_t limit_ns, unsigned int site,
                                            bool honour_abort = true) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_timer_ns();
-  uint32_t spins = 0;
-  while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((++spins & 63u) == 0) {
-      if (honour_abort && *reinterpret_cast<volatile uint32_t*>(&bars->abort_flag) != 0)
-        return false;
-      if (global_timer_ns() - t0 > limit_ns) {
-        *reinterpret_cast<volatile uint32_t*>(&bars->abort_flag) = 1u;
-        atomicOr(&g_sdpa_device_status, 1u | site);
-        return false;
-      }
-    }
-  }
+  return sdpa_sched::wait_phase(bar, parity, &bars->abort_flag, &g_sdpa_device_status, limit_ns,
+                                site, honour_abort);
 }
 
 // Warp-uniform version: every lane polls, and the warp proceeds only if all
@@ -199,352 +151,6 @@ __device__ __forceinline__ bool warp_wait_phase(uint64_t* bar, uint32_t parity, 
                                                 uint64_t limit_ns, unsigned int site) {
   const bool ok = wait_phase(bar, parity, bars, limit_ns, site);
   return __all_sync(0xffffffffu, ok);
-}
-
-__device__ __forceinline__ void tma_tile(void* dst, const CUtensorMap* map, uint64_t* bar,
-                                         int d0, int row, int head, int batch,
-                                         const int (&pos)[3]) {
-  // pos[] holds the map slot (1..3) of L, H and B; place the coordinates.
-  const int c1 = (pos[0] == 1) ? row : (pos[1] == 1) ? head : batch;
-  const int c2 = (pos[0] == 2) ? row : (pos[1] == 2) ? head : batch;
-  const int c3 = (pos[0] == 3) ? row : (pos[1] == 3) ? head : batch;
-  tma_load_4d(dst, map, bar, d0, c1, c2, c3);
-}
-
-template <bool BF16>
-__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
-  if constexpr (BF16) {
-    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<uint32_t*>(&v);
-  } else {
-    __half2 v = __floats2half2_rn(lo, hi);
-    return *reinterpret_cast<uint32_t*>(&v);
-  }
-}
-
-// Bit i (i = 0..3) set when byte i of `word` is nonzero: the bytes' sign
-// bits after a per-byte "!= 0" compare, gathered by one multiply (byte i's
-// bit 8i+7 times 2^(7(3-i)) lands on bit 28+i; every other product term
-// falls on a distinct bit outside 28..31, so nothing carries into them).
-__device__ __forceinline__ uint32_t nonzero_byte_bits(uint32_t word) {
-  const uint32_t m = __vcmpne4(word, 0u) & 0x80808080u;
-  return (m * 0x00204081u) >> 28;
-}
-
-// Work decomposition shared by every role of a CTA.  A job is one pair of
-// adjacent 128-row query tiles of one (sequence, head).  A unit is pair
-// P-1-k followed by pair k of the same head (P pairs per head): under the
-// causal mask the two cost 4P + 2 key tiles together whatever k is, so units
-// of one sequence length are equal and a static round-robin assignment of
-// units to persistent CTAs is balanced.  Units are numbered head-major, so
-// the CTAs busy at any moment work on a window of neighbouring heads whose
-// K/V stay in L2.  Every role walks the same sequence of jobs.
-struct Work {
-  int batch, head;         // tensor-map coordinates (batch is 0 for packed sequences)
-  int row0;                // first row of the sequence along L (packed: its offset)
-  int len;                 // rows (= keys) of the sequence
-  int tile[kTilesPerCta];  // query tile index of A and B within the sequence
-  int n_kv[kTilesPerCta];  // key tiles each query tile visits (0: tile absent)
-  int n_kv_max;
-};
-
-__host__ __device__ inline int pairs_per_head(int n_tiles) { return (n_tiles + 1) >> 1; }
-__host__ __device__ inline int units_per_head(int n_tiles) {
-  return (pairs_per_head(n_tiles) + 1) >> 1;
-}
-__host__ __device__ inline int tiles_of(int len) { return (len + kBlockM - 1) / kBlockM; }
-
-// Job `sub` (0 or 1) of unit k of one (sequence, head) with n_tiles tiles;
-// false when the unit has no such job (the middle pair of an odd pair count
-// stands alone).  Fills the tile fields of w.
-template <int MODE>
-__device__ __forceinline__ bool job_tiles(int n_tiles, int k, int sub, Work& w) {
-  const int P = pairs_per_head(n_tiles);
-  const int pr = (sub == 0) ? (P - 1 - k) : k;
-  if (sub == 1 && pr == P - 1 - k) return false;
-  w.n_kv_max = 0;
-#pragma unroll
-  for (int t = 0; t < kTilesPerCta; ++t) {
-    const int qt = 2 * pr + t;
-    w.tile[t] = qt;
-    w.n_kv[t] = (qt >= n_tiles) ? 0 : ((MODE == sdpa_impl::kMaskCausal) ? qt + 1 : n_tiles);
-    w.n_kv_max = max(w.n_kv_max, w.n_kv[t]);
-  }
-  return true;
-}
-
-// Packed sequences: a warp-wide cursor over cu_seqlens, 32 sequences per
-// step.  Lane i holds sequence chunk + i (its start and length and the
-// inclusive count of units up to it within the chunk); `before` counts the
-// units of earlier chunks.  Units are numbered sequence by sequence, each
-// sequence's heads in order.  With at most 32 sequences (one chunk) the
-// order is by cost instead, since any unit can then be found in the chunk:
-// first every sequence's two-job units, longest sequence first, then the
-// one-job units (the middle pair of an odd pair count), longest first, so the
-// snake deals the costly units before the cheap ones fill the gaps.  The offsets are used as the running maximum of
-// their values clamped to [0, total], so sequences never overlap and never
-// leave the buffers, whatever the array holds; for valid offsets (0 first,
-// nondecreasing, total last) that is the identity.  All 32 lanes run it.
-struct SeqCursor {
-  int chunk, before, chunk_units;
-  int carry;      // running-maximum offset where this chunk starts
-  int carry_out;  // ... and where it ends
-  int start, len, incl;
-  int incl_half, full_units;  // one chunk only: inclusive one-job units, all two-job units
-};
-
-__device__ __forceinline__ void cursor_load(const sdpa_impl::FwdParams& p, SeqCursor& c,
-                                            int lane) {
-  const int seq = c.chunk + lane;
-  int e = c.carry;
-  if (seq < p.n_seqs) e = max(e, min(max(__ldg(p.cu_seqlens + seq + 1), 0), p.L));
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const int v = __shfl_up_sync(0xffffffffu, e, off);
-    if (lane >= off) e = max(e, v);
-  }
-  int st = __shfl_up_sync(0xffffffffu, e, 1);
-  if (lane == 0) st = c.carry;
-  c.start = st;
-  c.len = e - st;
-  c.carry_out = __shfl_sync(0xffffffffu, e, 31);
-  if (p.n_seqs <= 32) {
-    // Bitonic sort of the lanes by (length, then lower index) descending;
-    // the keys are distinct, so every warp of every CTA gets one order.
-    uint64_t key = (static_cast<uint64_t>(c.len) << 6) | static_cast<uint64_t>(31 - lane);
-    int s0 = c.start;
-#pragma unroll
-    for (int kb = 2; kb <= 32; kb <<= 1) {
-#pragma unroll
-      for (int jb = kb >> 1; jb > 0; jb >>= 1) {
-        const uint64_t ok = __shfl_xor_sync(0xffffffffu, key, jb);
-        const int os = __shfl_xor_sync(0xffffffffu, s0, jb);
-        // the lower lane of a pair keeps the larger key in a descending run
-        const bool take = (((lane & jb) == 0) == ((lane & kb) == 0)) ? (ok > key) : (ok < key);
-        if (take) {
-          key = ok;
-          s0 = os;
-        }
-      }
-    }
-    c.start = s0;
-    c.len = static_cast<int>(key >> 6);
-    // two-job and one-job units of this sequence (per head: pairs / 2 and pairs % 2)
-    const int pairs = pairs_per_head(tiles_of(c.len));
-    int full = p.H * (pairs >> 1), half = p.H * (pairs & 1);
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const int vf = __shfl_up_sync(0xffffffffu, full, off);
-      const int vh = __shfl_up_sync(0xffffffffu, half, off);
-      if (lane >= off) {
-        full += vf;
-        half += vh;
-      }
-    }
-    c.incl = full;
-    c.incl_half = half;
-    c.full_units = __shfl_sync(0xffffffffu, full, 31);
-    c.chunk_units = c.full_units + __shfl_sync(0xffffffffu, half, 31);
-    return;
-  }
-  int incl = p.H * units_per_head(tiles_of(c.len));
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const int v = __shfl_up_sync(0xffffffffu, incl, off);
-    if (lane >= off) incl += v;
-  }
-  c.incl = incl;
-  c.chunk_units = __shfl_sync(0xffffffffu, incl, 31);
-}
-
-// Locates unit u (u only grows between calls).  False when u is past the
-// last unit.
-template <int MODE>
-__device__ __forceinline__ bool cursor_find(const sdpa_impl::FwdParams& p, SeqCursor& c, int lane,
-                                            int u, int& k, int& n_tiles, Work& w) {
-  while (u >= c.before + c.chunk_units) {
-    if (c.chunk + 32 >= p.n_seqs) return false;
-    c.before += c.chunk_units;
-    c.chunk += 32;
-    c.carry = c.carry_out;
-    cursor_load(p, c, lane);
-  }
-  if (p.n_seqs <= 32) {
-    // One chunk, ordered by cost: two-job units, then one-job units.
-    const bool half = u >= c.full_units;
-    const int rel = half ? u - c.full_units : u;
-    const unsigned hit = __ballot_sync(0xffffffffu, rel < (half ? c.incl_half : c.incl));
-    const int src = __ffs(static_cast<int>(hit)) - 1;
-    const int incl = __shfl_sync(0xffffffffu, half ? c.incl_half : c.incl, src);
-    const int len = __shfl_sync(0xffffffffu, c.len, src);
-    const int start = __shfl_sync(0xffffffffu, c.start, src);
-    n_tiles = tiles_of(len);
-    const int pairs = pairs_per_head(n_tiles);
-    w.batch = 0;
-    w.row0 = start;
-    w.len = len;
-    if (half) {
-      w.head = rel - (incl - p.H);  // one unit per head: the middle pair
-      k = pairs >> 1;
-    } else {
-      const int per_head = pairs >> 1;
-      const int r = rel - (incl - p.H * per_head);
-      w.head = r / per_head;
-      k = r - w.head * per_head;
-    }
-    return true;
-  }
-  const int rel = u - c.before;
-  const unsigned hit = __ballot_sync(0xffffffffu, rel < c.incl);
-  const int src = __ffs(static_cast<int>(hit)) - 1;
-  const int incl = __shfl_sync(0xffffffffu, c.incl, src);
-  const int len = __shfl_sync(0xffffffffu, c.len, src);
-  const int start = __shfl_sync(0xffffffffu, c.start, src);
-  n_tiles = tiles_of(len);
-  const int uph = units_per_head(n_tiles);
-  const int r = rel - (incl - p.H * uph);  // unit index within this sequence
-  w.batch = 0;
-  w.head = r / uph;
-  k = r - w.head * uph;
-  w.row0 = start;
-  w.len = len;
-  return true;
-}
-
-// Dense problems: the next job of this CTA (false at the end).  `it` is the
-// CTA's position; one call site per role keeps the roles' code single.
-//  * units (default): unit u = blockIdx.x, +gridDim.x, ...; its two jobs in
-//    turn (sub 0: pair P-1-k, sub 1: pair k);
-//  * snake (small problems whose heads' K and V all fit in L2): jobs in order
-//    of falling cost -- pair P-1 of every head, then pair P-2, ... -- dealt to
-//    the CTAs 0..G-1, then G-1..0, and so on, which balances unequal causal
-//    jobs far better than whole units when there are few jobs per CTA.
-struct DenseIter {
-  int u, sub;  // units
-  int r;       // snake round
-};
-
-template <int MODE>
-__device__ __forceinline__ bool dense_next(const sdpa_impl::FwdParams& p, DenseIter& it, Work& w) {
-  const int G = static_cast<int>(gridDim.x);
-  const int c = static_cast<int>(blockIdx.x);
-  const int BH = p.B * p.H;
-  w.row0 = 0;
-  w.len = p.L;
-  if (p.snake) {
-    const int P = pairs_per_head(p.n_tiles);
-    const int i = it.r * G + ((it.r & 1) ? G - 1 - c : c);
-    if (i >= BH * P) return false;
-    ++it.r;
-    const int cls = i / BH;
-    const int bh = i - cls * BH;
-    w.batch = bh / p.H;
-    w.head = bh - w.batch * p.H;
-    return job_tiles<MODE>(p.n_tiles, cls, 0, w);  // job 0 of unit k is pair P-1-k
-  }
-  const int uph = units_per_head(p.n_tiles);
-  while (it.u < BH * uph) {
-    const int bh = it.u / uph;
-    const int k = it.u - bh * uph;
-    const int sub = it.sub;
-    if (sub == 0) {
-      it.sub = 1;
-    } else {
-      it.sub = 0;
-      it.u += G;
-    }
-    w.batch = bh / p.H;
-    w.head = bh - w.batch * p.H;
-    if (job_tiles<MODE>(p.n_tiles, k, sub, w)) return true;
-  }
-  return false;
-}
-
-// Explicit mask with a tile summary: a job visits every key tile except
-// those whose every entry is removed for both of its query tiles.  Bit i of
-// the result: key tile 32 * chunk + i is visited (one ballot per 32 tiles;
-// every lane of the warp takes part).
-__device__ __forceinline__ uint32_t visit_chunk(const sdpa_impl::FwdParams& p, const Work& w,
-                                                int chunk) {
-  const int kt = chunk * 32 + static_cast<int>(threadIdx.x & 31);
-  bool visit = false;
-  if (kt < p.n_tiles) {
-#pragma unroll
-    for (int t = 0; t < kTilesPerCta; ++t)
-      visit = visit || (w.tile[t] < p.n_tiles &&
-                        __ldg(p.tile_class + static_cast<int64_t>(w.tile[t]) * p.n_tiles + kt) !=
-                            sdpa_impl::kTileRemoved);
-  }
-  return __ballot_sync(0xffffffffu, visit);
-}
-
-// n_kv of each present tile (and n_kv_max) becomes the number of visited key
-// tiles.  A job that visits none keeps n_kv = 0 for both tiles: the MMA and
-// load roles skip it and the softmax writes its rows as zeros.
-__device__ __forceinline__ void count_visits(const sdpa_impl::FwdParams& p, Work& w) {
-  int n = 0;
-  for (int c = 0; c * 32 < p.n_tiles; ++c) n += __popc(visit_chunk(p, w, c));
-#pragma unroll
-  for (int t = 0; t < kTilesPerCta; ++t) w.n_kv[t] = (w.n_kv[t] > 0) ? n : 0;
-  w.n_kv_max = n;
-}
-
-// The visited key tiles of one job in increasing order, one per call.
-struct KeyTileCursor {
-  int chunk;
-  uint32_t bits;  // visited tiles of `chunk` not yet returned
-};
-
-// Key tile of the j-th step of a job: j itself, or with a tile summary the
-// next visited tile (the cursor is called exactly n_kv_max times per job).
-template <int MODE>
-__device__ __forceinline__ int next_key_tile(const sdpa_impl::FwdParams& p, const Work& w,
-                                             KeyTileCursor& c, int j) {
-  if constexpr (MODE != sdpa_impl::kMaskExplicit) {
-    return j;
-  } else {
-    if (p.tile_class == nullptr) return j;
-    const int last = (p.n_tiles - 1) >> 5;
-    while (c.bits == 0u && c.chunk < last) c.bits = visit_chunk(p, w, ++c.chunk);
-    if (c.bits == 0u) return p.n_tiles - 1;  // not reached: n_kv_max tiles exist
-    const int kt = c.chunk * 32 + __ffs(static_cast<int>(c.bits)) - 1;
-    c.bits &= c.bits - 1u;
-    return kt;
-  }
-}
-
-// Calls f(work) for every job of this CTA, in order; stops when f returns
-// false.  VARLEN: packed sequences described by p.cu_seqlens.
-template <int MODE, bool VARLEN, typename F>
-__device__ __forceinline__ void for_each_job(const sdpa_impl::FwdParams& p, F&& f) {
-  if constexpr (!VARLEN) {
-    DenseIter it{static_cast<int>(blockIdx.x), 0, 0};
-    Work w;
-    while (dense_next<MODE>(p, it, w)) {
-      if constexpr (MODE == sdpa_impl::kMaskExplicit)
-        if (p.tile_class != nullptr) count_visits(p, w);
-      if (!f(w)) return;
-    }
-  } else {
-    const int step = static_cast<int>(gridDim.x);
-    const int lane = static_cast<int>(threadIdx.x & 31);
-    SeqCursor c{0, 0, 0, min(max(__ldg(p.cu_seqlens), 0), p.L), 0, 0, 0, 0};
-    cursor_load(p, c, lane);
-    // Units in snake order over the CTAs (0..G-1, then G-1..0, ...): units
-    // of different documents cost differently, and alternating the
-    // direction evens out what each CTA collects.  The sequence still grows,
-    // as the cursor needs.
-    const int cta = static_cast<int>(blockIdx.x);
-    for (int r = 0;; ++r) {
-      const int u = r * step + ((r & 1) ? step - 1 - cta : cta);
-      Work w;
-      int k, n_tiles;
-      if (!cursor_find<MODE>(p, c, lane, u, k, n_tiles, w)) return;
-#pragma unroll 1
-      for (int sub = 0; sub < 2; ++sub)
-        if (job_tiles<MODE>(n_tiles, k, sub, w) && !f(w)) return;
-    }
-  }
 }
 
 // ------------------------------------------------------------ softmax role
@@ -559,12 +165,12 @@ struct SoftmaxCounters {
 };
 
 // One job of one tile.  Returns false when a wait gave up.
-template <int D, int MODE, bool BF16>
-__device__ __forceinline__ bool softmax_job(const sdpa_impl::FwdParams& p, const Work& w, int t,
+template <int MODE, bool BF16>
+__device__ __forceinline__ bool softmax_job(const sdpa_impl::FwdParams& p, const Work<2>& w, int t,
                                             Barriers* bars, uint32_t tmem, int wq, int lane,
                                             SoftmaxCounters& cnt) {
-  const int n = t ? w.n_kv[1] : w.n_kv[0];
-  const int qt = t ? w.tile[1] : w.tile[0];
+  const int n = w.n_kv(t);
+  const int qt = w.tile(t);
   if (n == 0) {
     if constexpr (MODE == sdpa_impl::kMaskExplicit) {
       // A present tile whose job visits no key tile: every key of every
@@ -584,16 +190,14 @@ __device__ __forceinline__ bool softmax_job(const sdpa_impl::FwdParams& p, const
     return true;
   }
   const uint64_t limit = p.wait_limit_ns;
-  using Plan = TmemPlan<D>;
-  const uint32_t tS_base = tmem + (t ? Plan::s_col(1) : Plan::s_col(0));
-  const uint32_t tO_base = tmem + (t ? Plan::o_col(1) : Plan::o_col(0));
-  const uint32_t tP =
-      tmem + (t ? Plan::p_col(1) : Plan::p_col(0)) + (static_cast<uint32_t>(wq * 32) << 16);
+  const uint32_t tS_base = tmem + (t ? s_col(1) : s_col(0));
+  const uint32_t tO_base = tmem + (t ? o_col(1) : o_col(0));
   const int r = wq * 32 + lane;
   const int row_g = qt * kBlockM + r;
   const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
   const uint32_t tS = tS_base + lane_off;
   const uint32_t tO = tO_base + lane_off;
+  const uint32_t tP = tS;  // P_j is written over the first 64 columns of S_j
   const float sl2 = p.scale_log2;
   const bool pos_scale = sl2 >= 0.0f;
   const float mval = pos_scale ? -INFINITY : INFINITY;  // a removed raw score
@@ -605,7 +209,7 @@ __device__ __forceinline__ bool softmax_job(const sdpa_impl::FwdParams& p, const
   // are fetched one tile ahead, so the load's latency overlaps a whole tile
   // of work instead of the wait for S.  (A tile that removes nothing has
   // zero bits and skips the select below.)
-  int kt_next = next_key_tile<MODE>(p, w, kc, 0);
+  int kt_next = next_key_tile<MODE, 2>(p, w, kc, 0);
   uint4 bits_next = make_uint4(0u, 0u, 0u, 0u);
   const uint4* tile_bits_row = nullptr;
   if constexpr (MODE == sdpa_impl::kMaskExplicit) {
@@ -626,8 +230,6 @@ __device__ __forceinline__ bool softmax_job(const sdpa_impl::FwdParams& p, const
     // hides behind the score MMA.
     uint32_t mbits[kBlockN / 32];
     if constexpr (MODE == sdpa_impl::kMaskExplicit) {
-      const bool row_ok = row_g < w.len;
-      const uint8_t* mrow = p.mask + static_cast<int64_t>(row_ok ? row_g : 0) * p.L + col0;
       if (tile_bits_row != nullptr) {
         // Tile summary: the bits fetched during the previous tile (a warp
         // reads 512 contiguous bytes), and the next tile's now.
@@ -636,76 +238,11 @@ __device__ __forceinline__ bool softmax_job(const sdpa_impl::FwdParams& p, const
         mbits[2] = bits_next.z;
         mbits[3] = bits_next.w;
         if (j + 1 < n) {
-          kt_next = next_key_tile<MODE>(p, w, kc, j + 1);
+          kt_next = next_key_tile<MODE, 2>(p, w, kc, j + 1);
           bits_next = __ldg(tile_bits_row + static_cast<int64_t>(kt_next) * kBlockM);
         }
-      } else if (p.mask_vec16 && !tail && row_g - lane + 31 < w.len) {
-        static_assert(kBlockN == 128, "the mask transpose assumes 128-key tiles");
-        // Coalesced: lane (g, c) = (lane / 8, lane % 8) reads 16 bytes of
-        // row 8g + i at keys 16c.. for i = 0..7, so each load instruction
-        // covers four whole 128-byte row segments, and turns them into 16
-        // bits.  An 8 x 8 transpose of 16-bit values inside each group of
-        // eight lanes (three butterfly stages) then gives every lane the 128
-        // bits of its own row: word k = keys 32k..32k+31.
-        const int g8 = lane >> 3, c8 = lane & 7;
-        const uint8_t* mbase =
-            p.mask + static_cast<int64_t>(row_g - lane + 8 * g8) * p.L + col0 + 16 * c8;
-        uint4 x[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-          x[i] = __ldg(reinterpret_cast<const uint4*>(mbase + static_cast<int64_t>(i) * p.L));
-        uint32_t wv[4];
-#pragma unroll
-        for (int k2 = 0; k2 < 4; ++k2) {
-          const uint4 a = x[2 * k2], b = x[2 * k2 + 1];
-          const uint32_t ha = nonzero_byte_bits(a.x) | (nonzero_byte_bits(a.y) << 4) |
-                              (nonzero_byte_bits(a.z) << 8) | (nonzero_byte_bits(a.w) << 12);
-          const uint32_t hb = nonzero_byte_bits(b.x) | (nonzero_byte_bits(b.y) << 4) |
-                              (nonzero_byte_bits(b.z) << 8) | (nonzero_byte_bits(b.w) << 12);
-          wv[k2] = ha | (hb << 16);  // rows 8g+2k2 (low) and 8g+2k2+1 (high), keys 16c..
-        }
-        {  // swap the off-diagonal 4 x 4 blocks (lane bit 2 <-> element bit 2)
-          const bool hi = (c8 & 4) != 0;
-          const uint32_t r0 = __shfl_xor_sync(0xffffffffu, hi ? wv[0] : wv[2], 4);
-          const uint32_t r1 = __shfl_xor_sync(0xffffffffu, hi ? wv[1] : wv[3], 4);
-          if (hi) { wv[0] = r0; wv[1] = r1; } else { wv[2] = r0; wv[3] = r1; }
-        }
-        {  // 2 x 2 blocks inside each (lane bit 1 <-> element bit 1)
-          const bool hi = (c8 & 2) != 0;
-          const uint32_t r0 = __shfl_xor_sync(0xffffffffu, hi ? wv[0] : wv[1], 2);
-          const uint32_t r1 = __shfl_xor_sync(0xffffffffu, hi ? wv[2] : wv[3], 2);
-          if (hi) { wv[0] = r0; wv[2] = r1; } else { wv[1] = r0; wv[3] = r1; }
-        }
-        {  // single elements (lane bit 0 <-> the 16-bit half of a word)
-          const bool hi = (c8 & 1) != 0;
-          const uint32_t sel = hi ? 0x5410u : 0x7632u;
-          const uint32_t r0 = __shfl_xor_sync(0xffffffffu, __byte_perm(wv[0], wv[1], sel), 1);
-          const uint32_t r1 = __shfl_xor_sync(0xffffffffu, __byte_perm(wv[2], wv[3], sel), 1);
-          if (hi) {
-            wv[0] = __byte_perm(r0, wv[0], 0x7610u);
-            wv[1] = __byte_perm(r0, wv[1], 0x7632u);
-            wv[2] = __byte_perm(r1, wv[2], 0x7610u);
-            wv[3] = __byte_perm(r1, wv[3], 0x7632u);
-          } else {
-            wv[0] = __byte_perm(wv[0], r0, 0x5410u);
-            wv[1] = __byte_perm(wv[1], r0, 0x7610u);
-            wv[2] = __byte_perm(wv[2], r1, 0x5410u);
-            wv[3] = __byte_perm(wv[3], r1, 0x7610u);
-          }
-        }
-#pragma unroll
-        for (int k2 = 0; k2 < 4; ++k2) mbits[k2] = wv[k2];
       } else {
-#pragma unroll
-        for (int w32 = 0; w32 < kBlockN / 32; ++w32) {
-          uint32_t bits = 0;
-          for (int e = 0; e < 32; ++e) {
-            const int c = 32 * w32 + e;
-            const bool removed = !row_ok || col0 + c >= w.len || __ldg(mrow + c) != 0;
-            bits |= (removed ? 1u : 0u) << e;
-          }
-          mbits[w32] = bits;
-        }
+        mask_bits_from_bytes(p, w.len, row_g, lane, col0, mbits);
       }
       // A tile where none of this warp's 32 rows removes a key needs no
       // per-element select (warp-uniform, so structured masks skip it).
@@ -726,12 +263,6 @@ __device__ __forceinline__ bool softmax_job(const sdpa_impl::FwdParams& p, const
       tmem_ld_wait();
 #pragma unroll
       for (int c = 0; c < kBlockN; ++c) s[c] = __uint_as_float(su[c]);
-    }
-    if constexpr (Plan::kEarlyS) {
-      // S(j) is in registers: the MMA warp may overwrite it with S(j+1).
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->s_free[t]);
     }
     if (masked_tile) {
       if constexpr (MODE == sdpa_impl::kMaskExplicit) {
@@ -792,14 +323,7 @@ __device__ __forceinline__ bool softmax_job(const sdpa_impl::FwdParams& p, const
 #pragma unroll
     for (int c = 0; c < kBlockN; c += 2) fma2_bcast(s[c], s[c + 1], s[c], s[c + 1], sl2, neg_m);
 #pragma unroll
-    for (int c = 0; c < kBlockN; c += 2) {
-      if (poly_pair(c / 2)) {
-        ex2_poly2(s[c], s[c + 1], s[c], s[c + 1]);
-      } else {
-        s[c] = ex2(s[c]);
-        s[c + 1] = ex2(s[c + 1]);
-      }
-    }
+    for (int c = 0; c < kBlockN; ++c) s[c] = ex2(s[c]);
     uint32_t pk[kBlockN / 2];
     float rs[8];  // four packed pairs of partial row sums
 #pragma unroll
@@ -816,20 +340,9 @@ __device__ __forceinline__ bool softmax_job(const sdpa_impl::FwdParams& p, const
 
     if (j > 0) {
       // PV_{j-1} must have completed before O is rescaled or P_j replaces
-      // P_{j-1}.  Where P is written over S, S_j was issued after PV_{j-1}
-      // and the tensor pipe completes in issue order, so s_full(j) already
-      // implies it: that phase of o_done is complete and is only counted.
-      // Otherwise it is waited for here, in order and BEFORE the p_ready
-      // arrival below: once P_j is released PV_j may complete too, and a
-      // parity wait that falls two phases behind its barrier would block
-      // until the next phase (a timeout here) instead of returning.
-      if constexpr (Plan::kEarlyS) {
-        if (!warp_wait_phase(&bars->o_done[t], cnt.o_seen & 1, bars, limit, kSiteODone)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-      }
+      // P_{j-1}: S_j was issued after PV_{j-1} and the tensor pipe completes
+      // in issue order, so s_full(j) already implies it -- that phase of
+      // o_done is complete and is only counted here.
       ++cnt.o_seen;
       if (__any_sync(0xffffffffu, need)) {
 #pragma unroll
@@ -844,9 +357,8 @@ __device__ __forceinline__ bool softmax_job(const sdpa_impl::FwdParams& p, const
         }
       }
     }
-    // P_j goes into the P buffer -- the first 64 columns of this tile's score
-    // buffer, or its own buffer in the early-S plan (free again: PV_{j-1}
-    // has completed, see above).
+    // P_j goes into the first 64 columns of this tile's score buffer (free
+    // again: PV_{j-1} has completed, see above).
     tmem_st32(tP + 0, pk);
     tmem_st32(tP + 32, pk + 32);
     tmem_st_wait();
@@ -897,10 +409,10 @@ __device__ __forceinline__ bool softmax_job(const sdpa_impl::FwdParams& p, const
 }
 
 // ------------------------------------------------------------------ kernel
-template <int D, int MODE, bool BF16, bool VARLEN>
+template <int MODE, bool BF16, bool VARLEN>
 __global__ void __launch_bounds__(kThreads, 1)
     sdpa_fwd_kernel(const __grid_constant__ sdpa_impl::FwdParams p) {
-  using Lay = Layout<D>;
+  using Lay = Layout;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -921,7 +433,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->s_full[t], 1);
       mbar_init(&bars->p_ready[t], kBlockM / 32);
       mbar_init(&bars->o_done[t], 1);
-      mbar_init(&bars->s_free[t], kBlockM / 32);
       mbar_init(&bars->o_free[t], kBlockM / 32);
     }
     mbar_init(&bars->fin, 1);
@@ -956,12 +467,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   grid_dependency_wait();
   grid_launch_dependents();
   const uint32_t tmem = bars->tmem_base;
-  // TMEM columns: S_A [0,128), S_B [128,256), O_A [256, 256+D), O_B [256+D, 256+2D),
-  // and with D = 64 also P_A [384, 448), P_B [448, 512).
-  using Plan = TmemPlan<D>;
-  const uint32_t tS[kTilesPerCta] = {tmem + Plan::s_col(0), tmem + Plan::s_col(1)};
-  const uint32_t tO[kTilesPerCta] = {tmem + Plan::o_col(0), tmem + Plan::o_col(1)};
-  const uint32_t tPv[kTilesPerCta] = {tmem + Plan::p_col(0), tmem + Plan::p_col(1)};
+  const uint32_t tS[kTilesPerCta] = {tmem + s_col(0), tmem + s_col(1)};
+  const uint32_t tO[kTilesPerCta] = {tmem + o_col(0), tmem + o_col(1)};
 
   if (warp >= 4) {
     // ------------------------------------------- softmax / output warps
@@ -969,8 +476,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // warps 4..7 -> tile A, 8..11 -> tile B; the same jobs as the other roles
     const int t = (warp - 4) >> 2;
     SoftmaxCounters cnt{0, 0};
-    for_each_job<MODE, VARLEN>(p, [&](const Work& w) {
-      return softmax_job<D, MODE, BF16>(p, w, t, bars, tmem, warp & 3, lane, cnt);
+    for_each_job<MODE, VARLEN, kTilesPerCta>(p, [&](const Work<kTilesPerCta>& w) {
+      return softmax_job<MODE, BF16>(p, w, t, bars, tmem, warp & 3, lane, cnt);
     });
   } else {
     regs_decrease<kRegsControl>();
@@ -984,19 +491,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Key/value tiles issued so far over all jobs (ring position) and jobs
     // whose Q was loaded; a give-up drains what was issued.
     int g = 0, k_end = 0, v_end = 0, jobs = 0;
-    for_each_job<MODE, VARLEN>(p, [&](const Work& w) -> bool {
+    for_each_job<MODE, VARLEN, kTilesPerCta>(p, [&](const Work<kTilesPerCta>& w) -> bool {
       if (w.n_kv_max == 0) return true;  // masked out entirely: nothing to load
       // The previous job's Q must be consumed (all its S products done).
       if (jobs > 0 && !warp_wait_phase(&bars->q_empty, (jobs - 1) & 1, bars, limit, kSiteEmpty))
         return false;
       if (!p.debug_withhold_q && leader) {
-        const int nq = (w.n_kv[1] > 0) ? 2 : 1;
+        const int nq = w.n_present;
         mbar_arrive_expect_tx(&bars->q_full, nq * Lay::kTileBytes);
         for (int t = 0; t < nq; ++t)
 #pragma unroll
           for (int c = 0; c < Lay::kChunks; ++c)
             tma_tile(sQ + t * Lay::kTileBytes + c * Lay::kChunkBytes, &p.tm_q, &bars->q_full,
-                     c * 64, w.row0 + w.tile[t] * kBlockM, w.head, w.batch, p.pos_q);
+                     c * 64, w.row0 + w.tile(t) * kBlockM, w.head, w.batch, p.pos_q);
       }
       ++jobs;
       // Key tiles in order; with a mask summary every tile is examined and
@@ -1006,7 +513,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t visit = 0xffffffffu;
       for (int kt = 0; kt < n_scan; ++kt) {
         if (summary) {
-          if ((kt & 31) == 0) visit = visit_chunk(p, w, kt >> 5);
+          if ((kt & 31) == 0) visit = visit_chunk<kTilesPerCta>(p, w, kt >> 5);
           if (((visit >> (kt & 31)) & 1u) == 0u) continue;
         }
         const int s = g % Lay::kKStages;
@@ -1081,7 +588,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto issue_pv = [&](int t, int s, bool accumulate) {
       const uint32_t b0 = v_lo + static_cast<uint32_t>(s * (Lay::kTileBytes >> 4));
       const uint32_t d = t ? tO[1] : tO[0];
-      const uint32_t a = t ? tPv[1] : tPv[0];
+      const uint32_t a = t ? tS[1] : tS[0];  // P_t over the first 64 columns of S_t
 #pragma unroll
       for (int kk = 0; kk < kBlockN / 16; ++kk) {
         // keys kk*16 .. +16: 16 rows of 128 B
@@ -1092,12 +599,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
 
     // Running counters over all jobs: ring position g, jobs done, P-ready
-    // phases consumed per tile, jobs per tile (for o_free), and in the
-    // early-S plan the S(j) loads consumed per tile.
+    // phases consumed per tile and jobs per tile (for o_free).
     int g = 0, jobs = 0;
     uint32_t p_seen[kTilesPerCta] = {0, 0}, t_jobs[kTilesPerCta] = {0, 0};
-    uint32_t f_seen[kTilesPerCta] = {0, 0};
-    for_each_job<MODE, VARLEN>(p, [&](const Work& w) -> bool {
+    for_each_job<MODE, VARLEN, kTilesPerCta>(p, [&](const Work<kTilesPerCta>& w) -> bool {
       if (w.n_kv_max == 0) return true;  // masked out entirely: no products
       if (!warp_wait_phase(&bars->q_full, jobs & 1, bars, limit, kSiteQFull) ||
           !warp_wait_phase(&bars->k_full[g % Lay::kKStages], (g / Lay::kKStages) & 1, bars, limit,
@@ -1106,16 +611,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
 #pragma unroll
       for (int t = 0; t < kTilesPerCta; ++t) {
-        if (w.n_kv[t] == 0) continue;
-        if constexpr (Plan::kEarlyS) {
-          // The previous job's last S_t must be in its softmax's registers.
-          if (t_jobs[t] > 0) {
-            if (!warp_wait_phase(&bars->s_free[t], f_seen[t] & 1, bars, limit, kSiteSFree))
-              return false;
-            ++f_seen[t];
-            tc_fence_after();
-          }
-        }
+        if (w.n_kv(t) == 0) continue;
         issue_s(t, g % Lay::kKStages);
       }
       mma_commit_elect(&bars->k_empty[g % Lay::kKStages]);
@@ -1142,30 +638,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int s1 = (gj + 1) % Lay::kKStages;  // K(j+1)
         const uint32_t ph1 = ((gj + 1) / Lay::kKStages) & 1;
         bool k_next = false;
-        if constexpr (Plan::kEarlyS) {
-          // S(j+1) of both tiles first (each once its softmax has loaded
-          // S(j)), then PV(j) of both tiles as their P(j) become ready.
-#pragma unroll
-          for (int t = 0; t < kTilesPerCta; ++t) {
-            if (j + 1 >= w.n_kv[t]) continue;
-            if (!k_next) {
-              if (!warp_wait_phase(&bars->k_full[s1], ph1, bars, limit, kSiteKFull)) {
-                ok = false;
-                break;
-              }
-              k_next = true;
-            }
-            if (!warp_wait_phase(&bars->s_free[t], f_seen[t] & 1, bars, limit, kSiteSFree)) {
-              ok = false;
-              break;
-            }
-            ++f_seen[t];
-            tc_fence_after();
-            issue_s(t, s1);
-          }
-          if (!ok) break;
-          if (k_next) mma_commit_elect(&bars->k_empty[s1]);
-          if (j + 2 == w.n_kv_max) mma_commit_elect(&bars->q_empty);  // job's last S issued
+        {
           if (!warp_wait_phase(&bars->v_full[s], (gj / Lay::kVStages) & 1, bars, limit,
                                kSiteVFull)) {
             ok = false;
@@ -1173,30 +646,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
 #pragma unroll
           for (int t = 0; t < kTilesPerCta; ++t) {
-            if (j >= w.n_kv[t]) continue;
+            if (j >= w.n_kv(t)) continue;
             if (!pv_ready(t, j)) {
               ok = false;
               break;
             }
             issue_pv(t, s, j > 0);
-          }
-          if (!ok) break;
-          mma_commit_elect(&bars->v_empty[s]);
-        } else {
-          if (!warp_wait_phase(&bars->v_full[s], (gj / Lay::kVStages) & 1, bars, limit,
-                               kSiteVFull)) {
-            ok = false;
-            break;
-          }
-#pragma unroll
-          for (int t = 0; t < kTilesPerCta; ++t) {
-            if (j >= w.n_kv[t]) continue;
-            if (!pv_ready(t, j)) {
-              ok = false;
-              break;
-            }
-            issue_pv(t, s, j > 0);
-            if (j + 1 < w.n_kv[t]) {
+            if (j + 1 < w.n_kv(t)) {
               if (!k_next) {
                 if (!warp_wait_phase(&bars->k_full[s1], ph1, bars, limit, kSiteKFull)) {
                   ok = false;
@@ -1219,7 +675,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++jobs;
 #pragma unroll
       for (int t = 0; t < kTilesPerCta; ++t)
-        if (w.n_kv[t] > 0) ++t_jobs[t];
+        if (w.n_kv(t) > 0) ++t_jobs[t];
       return true;
     });
     if (issued_any) {
@@ -1238,10 +694,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D, int MODE, bool BF16, bool VARLEN>
+template <int MODE, bool BF16, bool VARLEN>
 cudaError_t launch_one(const sdpa_impl::FwdParams& p, int max_ctas, cudaStream_t stream) {
-  auto kern = sdpa_fwd_kernel<D, MODE, BF16, VARLEN>;
-  constexpr int smem = Layout<D>::kTotal;
+  auto kern = sdpa_fwd_kernel<MODE, BF16, VARLEN>;
+  constexpr int smem = Layout::kTotal;
   static bool configured = false;  // one attribute call per instantiation
   if (!configured) {
     // The in-kernel register split assumes the launch reserves kLaunchRegs
@@ -1257,13 +713,7 @@ cudaError_t launch_one(const sdpa_impl::FwdParams& p, int max_ctas, cudaStream_t
   }
   // Persistent grid: one CTA per SM at most, each walking its share of the
   // equal-cost units.
-  const long long n_units =
-      VARLEN ? p.max_units
-             : static_cast<long long>(p.B) * p.H *
-                   (p.snake ? pairs_per_head(p.n_tiles) : units_per_head(p.n_tiles));
-  long long g = n_units < static_cast<long long>(max_ctas) ? n_units : max_ctas;
-  if (g < 1) g = 1;
-  const unsigned grid = static_cast<unsigned>(g);
+  const unsigned grid = grid_size<kTilesPerCta>(p, VARLEN, max_ctas);
   // Programmatic dependent launch: this grid's set-up may start while the
   // previous kernel in the stream drains; the kernel waits for it
   // (griddepcontrol.wait) before its first global-memory access.
@@ -1280,22 +730,22 @@ cudaError_t launch_one(const sdpa_impl::FwdParams& p, int max_ctas, cudaStream_t
   return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
-template <int D, bool BF16>
+template <bool BF16>
 cudaError_t launch_mode(const sdpa_impl::FwdParams& p, int mode, int max_ctas,
                         cudaStream_t stream) {
   if (p.cu_seqlens != nullptr) {  // packed sequences: causal or no mask
     if (mode == sdpa_impl::kMaskExplicit) return cudaErrorInvalidValue;
     return mode == sdpa_impl::kMaskCausal
-               ? launch_one<D, sdpa_impl::kMaskCausal, BF16, true>(p, max_ctas, stream)
-               : launch_one<D, sdpa_impl::kMaskNone, BF16, true>(p, max_ctas, stream);
+               ? launch_one<sdpa_impl::kMaskCausal, BF16, true>(p, max_ctas, stream)
+               : launch_one<sdpa_impl::kMaskNone, BF16, true>(p, max_ctas, stream);
   }
   switch (mode) {
     case sdpa_impl::kMaskCausal:
-      return launch_one<D, sdpa_impl::kMaskCausal, BF16, false>(p, max_ctas, stream);
+      return launch_one<sdpa_impl::kMaskCausal, BF16, false>(p, max_ctas, stream);
     case sdpa_impl::kMaskExplicit:
-      return launch_one<D, sdpa_impl::kMaskExplicit, BF16, false>(p, max_ctas, stream);
+      return launch_one<sdpa_impl::kMaskExplicit, BF16, false>(p, max_ctas, stream);
     default:
-      return launch_one<D, sdpa_impl::kMaskNone, BF16, false>(p, max_ctas, stream);
+      return launch_one<sdpa_impl::kMaskNone, BF16, false>(p, max_ctas, stream);
   }
 }
 
@@ -1346,32 +796,9 @@ __global__ void __launch_bounds__(256) mask_tiles_kernel(const sdpa_impl::MaskTi
         !removed ? sdpa_impl::kTileKept : (!kept ? sdpa_impl::kTileRemoved : sdpa_impl::kTileMixed);
 }
 
-// Test hook: y = 2^x through the FMA-pipe polynomial (pairs of elements).
-__global__ void exp2_poly_kernel(const float* x, float* y, int64_t n) {
-  const int64_t i = 2 * (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x);
-  if (i + 1 < n) {
-    float a, b;
-    ex2_poly2(a, b, x[i], x[i + 1]);
-    y[i] = a;
-    y[i + 1] = b;
-  } else if (i < n) {
-    float a, b;
-    ex2_poly2(a, b, x[i], 0.0f);
-    y[i] = a;
-  }
-}
-
 }  // namespace
 
 namespace sdpa_impl {
-
-cudaError_t launch_exp2_poly(const float* x, float* y, int64_t n, cudaStream_t stream) {
-  if (n <= 0) return cudaSuccess;
-  const int64_t pairs = (n + 1) / 2;
-  const unsigned blocks = static_cast<unsigned>((pairs + 255) / 256);
-  exp2_poly_kernel<<<blocks, 256, 0, stream>>>(x, y, n);
-  return cudaGetLastError();
-}
 
 cudaError_t launch_mask_tiles(const MaskTilesParams& p, cudaStream_t stream) {
   if (p.n_tiles < 1 || p.n_tiles > 65535) return cudaErrorInvalidValue;
@@ -1391,11 +818,9 @@ cudaError_t launch_mask_tiles(const MaskTilesParams& p, cudaStream_t stream) {
 cudaError_t launch_forward(const FwdParams& p, int head_dim, int mask_mode, bool bf16,
                            int max_ctas, cudaStream_t stream) {
   if (max_ctas < 1) return cudaErrorInvalidValue;
-  if (head_dim == 64)
-    return bf16 ? launch_mode<64, true>(p, mask_mode, max_ctas, stream)
-                : launch_mode<64, false>(p, mask_mode, max_ctas, stream);
-  return bf16 ? launch_mode<128, true>(p, mask_mode, max_ctas, stream)
-              : launch_mode<128, false>(p, mask_mode, max_ctas, stream);
+  if (head_dim == 64) return launch_forward64(p, mask_mode, bf16, max_ctas, stream);
+  return bf16 ? launch_mode<true>(p, mask_mode, max_ctas, stream)
+              : launch_mode<false>(p, mask_mode, max_ctas, stream);
 }
 
 cudaError_t noalloc_mask_tiles(int device, const uint4** tile_bits,

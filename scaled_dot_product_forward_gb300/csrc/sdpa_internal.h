@@ -99,8 +99,12 @@ enum MaskMode : int { kMaskNone = 0, kMaskCausal = 1, kMaskExplicit = 2 };
 // count).  Returns the CUDA error of the launch.
 cudaError_t launch_forward(const FwdParams& p, int head_dim, int mask_mode, bool bf16,
                            int max_ctas, cudaStream_t stream);
+// The head-size-64 kernel (its own translation unit; launch_forward calls it).
+cudaError_t launch_forward64(const FwdParams& p, int mask_mode, bool bf16, int max_ctas,
+                             cudaStream_t stream);
+// Reads and clears the head-size-64 kernel's status word.
+cudaError_t read_and_clear_fwd64_status(unsigned int* status);
 
-// Test hook: y[i] = 2^x[i] through the kernel's FMA-pipe polynomial.
 // Writes the tile summary of p.mask (PDL launch: waits for the previous
 // kernel in the stream before reading the mask).
 cudaError_t launch_mask_tiles(const MaskTilesParams& p, cudaStream_t stream);
@@ -112,8 +116,6 @@ cudaError_t launch_mask_tiles(const MaskTilesParams& p, cudaStream_t stream);
 constexpr int kNoAllocMaxTiles = 32;
 constexpr int kNoAllocMaxDevices = 64;
 cudaError_t noalloc_mask_tiles(int device, const uint4** tile_bits, const uint8_t** tile_class);
-
-cudaError_t launch_exp2_poly(const float* x, float* y, int64_t n, cudaStream_t stream);
 
 // Reads and clears the device status word (nonzero = a barrier wait timed out).
 cudaError_t read_and_clear_device_status(cudaStream_t stream, unsigned int* status);

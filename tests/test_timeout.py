@@ -14,8 +14,9 @@ import sdpa_inputs
 pytestmark = pytest.mark.gpu
 
 
-def test_withheld_load_times_out_and_recovers(sdpa_lib):
-    q, k, v = sdpa_inputs.custom((1, 1, 256, 128), seed=21)
+@pytest.mark.parametrize("D", [128, 64])
+def test_withheld_load_times_out_and_recovers(sdpa_lib, D):
+    q, k, v = sdpa_inputs.custom((1, 1, 256, D), seed=21)
     qd, kd, vd = (x.cuda() for x in (q, k, v))
     assert sdpa_lib.sdpa_last_device_status()[0] == 0
     try:
