@@ -79,81 +79,104 @@ __device__ __forceinline__ uint32_t nonzero_byte_bits(uint32_t word) {
 
 // The 128 mask bits (bit set = key removed) of this thread's row for the
 // 128-key tile starting at col0, read from the byte mask: word k = keys
-// 32k..32k+31.  All 32 lanes of the warp call it with consecutive rows
+// 32k..32k+31.  All 32 lanes of the warp take part, with consecutive rows
 // (row_g - lane is the warp's first row).  When the warp's 32 rows and the
-// 128 keys all lie inside [len, len] and rows may be read as 16-byte vectors,
-// lane (g, c) = (lane / 8, lane % 8) reads 16 bytes of row 8g + i at keys
-// 16c.. for i = 0..7, so each load instruction covers four whole 128-byte
-// row segments, and turns them into 16 bits; an 8 x 8 transpose of 16-bit
-// values inside each group of eight lanes (three butterfly stages) then
-// gives every lane the 128 bits of its own row.  Otherwise each row is read
-// byte by byte, with rows and keys past len counted as removed.
+// 128 keys all lie inside [len, len] and rows may be read as 16-byte vectors
+// (mask_vec_ok), lane (g, c) = (lane / 8, lane % 8) reads 16 bytes of row
+// 8g + i at keys 16c.. for i = 0..7 (mask_bytes_load), so each load
+// instruction covers four whole 128-byte row segments, and mask_bits_convert
+// turns them into 16 bits and then, with an 8 x 8 transpose of 16-bit values
+// inside each group of eight lanes (three butterfly stages), into the 128
+// bits of each lane's own row.  The two halves may be split so that the
+// loads of one tile are in flight while the previous tile is worked on.
+// Otherwise (mask_bits_slow) each row is read byte by byte, with rows and
+// keys past len counted as removed.
+__device__ __forceinline__ bool mask_vec_ok(const sdpa_impl::FwdParams& p, int len, int row_g,
+                                            int lane, int col0) {
+  return p.mask_vec16 && col0 + kBlockN <= len && row_g - lane + 31 < len;
+}
+
+__device__ __forceinline__ void mask_bytes_load(const sdpa_impl::FwdParams& p, int row_g,
+                                                int lane, int col0, uint4 (&x)[8]) {
+  const int g8 = lane >> 3, c8 = lane & 7;
+  const uint8_t* mbase =
+      p.mask + static_cast<int64_t>(row_g - lane + 8 * g8) * p.L + col0 + 16 * c8;
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    x[i] = __ldg(reinterpret_cast<const uint4*>(mbase + static_cast<int64_t>(i) * p.L));
+}
+
+__device__ __forceinline__ void mask_bits_convert(const uint4 (&x)[8], int lane,
+                                                  uint32_t (&mbits)[4]) {
+  const int c8 = lane & 7;
+  uint32_t wv[4];
+#pragma unroll
+  for (int k2 = 0; k2 < 4; ++k2) {
+    const uint4 a = x[2 * k2], b = x[2 * k2 + 1];
+    const uint32_t ha = nonzero_byte_bits(a.x) | (nonzero_byte_bits(a.y) << 4) |
+                        (nonzero_byte_bits(a.z) << 8) | (nonzero_byte_bits(a.w) << 12);
+    const uint32_t hb = nonzero_byte_bits(b.x) | (nonzero_byte_bits(b.y) << 4) |
+                        (nonzero_byte_bits(b.z) << 8) | (nonzero_byte_bits(b.w) << 12);
+    wv[k2] = ha | (hb << 16);  // rows 8g+2k2 (low) and 8g+2k2+1 (high), keys 16c..
+  }
+  {  // swap the off-diagonal 4 x 4 blocks (lane bit 2 <-> element bit 2)
+    const bool hi = (c8 & 4) != 0;
+    const uint32_t r0 = __shfl_xor_sync(0xffffffffu, hi ? wv[0] : wv[2], 4);
+    const uint32_t r1 = __shfl_xor_sync(0xffffffffu, hi ? wv[1] : wv[3], 4);
+    if (hi) { wv[0] = r0; wv[1] = r1; } else { wv[2] = r0; wv[3] = r1; }
+  }
+  {  // 2 x 2 blocks inside each (lane bit 1 <-> element bit 1)
+    const bool hi = (c8 & 2) != 0;
+    const uint32_t r0 = __shfl_xor_sync(0xffffffffu, hi ? wv[0] : wv[1], 2);
+    const uint32_t r1 = __shfl_xor_sync(0xffffffffu, hi ? wv[2] : wv[3], 2);
+    if (hi) { wv[0] = r0; wv[2] = r1; } else { wv[1] = r0; wv[3] = r1; }
+  }
+  {  // single elements (lane bit 0 <-> the 16-bit half of a word)
+    const bool hi = (c8 & 1) != 0;
+    const uint32_t sel = hi ? 0x5410u : 0x7632u;
+    const uint32_t r0 = __shfl_xor_sync(0xffffffffu, __byte_perm(wv[0], wv[1], sel), 1);
+    const uint32_t r1 = __shfl_xor_sync(0xffffffffu, __byte_perm(wv[2], wv[3], sel), 1);
+    if (hi) {
+      wv[0] = __byte_perm(r0, wv[0], 0x7610u);
+      wv[1] = __byte_perm(r0, wv[1], 0x7632u);
+      wv[2] = __byte_perm(r1, wv[2], 0x7610u);
+      wv[3] = __byte_perm(r1, wv[3], 0x7632u);
+    } else {
+      wv[0] = __byte_perm(wv[0], r0, 0x5410u);
+      wv[1] = __byte_perm(wv[1], r0, 0x7610u);
+      wv[2] = __byte_perm(wv[2], r1, 0x5410u);
+      wv[3] = __byte_perm(wv[3], r1, 0x7610u);
+    }
+  }
+#pragma unroll
+  for (int k2 = 0; k2 < 4; ++k2) mbits[k2] = wv[k2];
+}
+
+__device__ __forceinline__ void mask_bits_slow(const sdpa_impl::FwdParams& p, int len, int row_g,
+                                               int col0, uint32_t (&mbits)[4]) {
+  const bool row_ok = row_g < len;
+  const uint8_t* mrow = p.mask + static_cast<int64_t>(row_ok ? row_g : 0) * p.L + col0;
+#pragma unroll
+  for (int w32 = 0; w32 < kBlockN / 32; ++w32) {
+    uint32_t bits = 0;
+    for (int e = 0; e < 32; ++e) {
+      const int c = 32 * w32 + e;
+      const bool removed = !row_ok || col0 + c >= len || __ldg(mrow + c) != 0;
+      bits |= (removed ? 1u : 0u) << e;
+    }
+    mbits[w32] = bits;
+  }
+}
+
 __device__ __forceinline__ void mask_bits_from_bytes(const sdpa_impl::FwdParams& p, int len,
                                                      int row_g, int lane, int col0,
                                                      uint32_t (&mbits)[4]) {
-  const bool tail = col0 + kBlockN > len;
-  if (p.mask_vec16 && !tail && row_g - lane + 31 < len) {
-    const int g8 = lane >> 3, c8 = lane & 7;
-    const uint8_t* mbase =
-        p.mask + static_cast<int64_t>(row_g - lane + 8 * g8) * p.L + col0 + 16 * c8;
+  if (mask_vec_ok(p, len, row_g, lane, col0)) {
     uint4 x[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-      x[i] = __ldg(reinterpret_cast<const uint4*>(mbase + static_cast<int64_t>(i) * p.L));
-    uint32_t wv[4];
-#pragma unroll
-    for (int k2 = 0; k2 < 4; ++k2) {
-      const uint4 a = x[2 * k2], b = x[2 * k2 + 1];
-      const uint32_t ha = nonzero_byte_bits(a.x) | (nonzero_byte_bits(a.y) << 4) |
-                          (nonzero_byte_bits(a.z) << 8) | (nonzero_byte_bits(a.w) << 12);
-      const uint32_t hb = nonzero_byte_bits(b.x) | (nonzero_byte_bits(b.y) << 4) |
-                          (nonzero_byte_bits(b.z) << 8) | (nonzero_byte_bits(b.w) << 12);
-      wv[k2] = ha | (hb << 16);  // rows 8g+2k2 (low) and 8g+2k2+1 (high), keys 16c..
-    }
-    {  // swap the off-diagonal 4 x 4 blocks (lane bit 2 <-> element bit 2)
-      const bool hi = (c8 & 4) != 0;
-      const uint32_t r0 = __shfl_xor_sync(0xffffffffu, hi ? wv[0] : wv[2], 4);
-      const uint32_t r1 = __shfl_xor_sync(0xffffffffu, hi ? wv[1] : wv[3], 4);
-      if (hi) { wv[0] = r0; wv[1] = r1; } else { wv[2] = r0; wv[3] = r1; }
-    }
-    {  // 2 x 2 blocks inside each (lane bit 1 <-> element bit 1)
-      const bool hi = (c8 & 2) != 0;
-      const uint32_t r0 = __shfl_xor_sync(0xffffffffu, hi ? wv[0] : wv[1], 2);
-      const uint32_t r1 = __shfl_xor_sync(0xffffffffu, hi ? wv[2] : wv[3], 2);
-      if (hi) { wv[0] = r0; wv[2] = r1; } else { wv[1] = r0; wv[3] = r1; }
-    }
-    {  // single elements (lane bit 0 <-> the 16-bit half of a word)
-      const bool hi = (c8 & 1) != 0;
-      const uint32_t sel = hi ? 0x5410u : 0x7632u;
-      const uint32_t r0 = __shfl_xor_sync(0xffffffffu, __byte_perm(wv[0], wv[1], sel), 1);
-      const uint32_t r1 = __shfl_xor_sync(0xffffffffu, __byte_perm(wv[2], wv[3], sel), 1);
-      if (hi) {
-        wv[0] = __byte_perm(r0, wv[0], 0x7610u);
-        wv[1] = __byte_perm(r0, wv[1], 0x7632u);
-        wv[2] = __byte_perm(r1, wv[2], 0x7610u);
-        wv[3] = __byte_perm(r1, wv[3], 0x7632u);
-      } else {
-        wv[0] = __byte_perm(wv[0], r0, 0x5410u);
-        wv[1] = __byte_perm(wv[1], r0, 0x7610u);
-        wv[2] = __byte_perm(wv[2], r1, 0x5410u);
-        wv[3] = __byte_perm(wv[3], r1, 0x7610u);
-      }
-    }
-#pragma unroll
-    for (int k2 = 0; k2 < 4; ++k2) mbits[k2] = wv[k2];
+    mask_bytes_load(p, row_g, lane, col0, x);
+    mask_bits_convert(x, lane, mbits);
   } else {
-    const bool row_ok = row_g < len;
-    const uint8_t* mrow = p.mask + static_cast<int64_t>(row_ok ? row_g : 0) * p.L + col0;
-#pragma unroll
-    for (int w32 = 0; w32 < kBlockN / 32; ++w32) {
-      uint32_t bits = 0;
-      for (int e = 0; e < 32; ++e) {
-        const int c = 32 * w32 + e;
-        const bool removed = !row_ok || col0 + c >= len || __ldg(mrow + c) != 0;
-        bits |= (removed ? 1u : 0u) << e;
-      }
-      mbits[w32] = bits;
-    }
+    mask_bits_slow(p, len, row_g, col0, mbits);
   }
 }
 
