@@ -78,12 +78,17 @@ constexpr uint32_t kColS0 = 0, kColO = 256, kColP = 384, kTmemCols = 512;
 constexpr int kMaxStages = 12;
 struct SBarriers {
   uint64_t q_full, q_empty;
-  uint64_t s_full[2], s_free[2];
+  // S buffer b is refilled only after the product of the tile two before,
+  // whose P the softmax stored after loading that tile's S: no release
+  // barrier of its own
+  uint64_t s_full[2];
   // P and O += P V double-buffered by tile parity: tile t uses P buffer t & 1,
   // p_ready[t & 1] and o_done[t & 1] (each completes once per two tiles).
   uint64_t p_ready[2], o_done[2], o_free, fin;
   uint64_t k_full[kMaxStages], k_empty[kMaxStages];
-  uint64_t v_full[kMaxStages], v_empty[kMaxStages];
+  // (a stage's K and V rows are copied as one group and announced together
+  // by k_full)
+  uint64_t v_empty[kMaxStages];
   // Validity of the 128 gathered keys of K tile g, in slot g % kMaskSlots:
   // word w bit i = key 32w + i; m_full[slot] completes when both gather
   // warps have written their words.
@@ -96,10 +101,11 @@ static_assert(sizeof(SBarriers) <= 1024, "barrier block too large");
 
 enum SparseSite : unsigned int {
   kSpQ = 1u << 1, kSpK = 1u << 2, kSpEmpty = 1u << 3, kSpS = 1u << 4, kSpP = 1u << 5,
-  kSpO = 1u << 6, kSpDrain = 1u << 7, kSpV = 1u << 8, kSpSFree = 1u << 9,
+  kSpO = 1u << 6, kSpDrain = 1u << 7,
 };
 
-__device__ __forceinline__ bool swait(uint64_t* bar, uint32_t parity, SBarriers* bars,
+template <class Bars>
+__device__ __forceinline__ bool swait(uint64_t* bar, uint32_t parity, Bars* bars,
                                       uint64_t limit_ns, unsigned int site,
                                       bool honour_abort = true) {
   if (mbar_try_wait(bar, parity)) return true;
@@ -118,7 +124,8 @@ __device__ __forceinline__ bool swait(uint64_t* bar, uint32_t parity, SBarriers*
     }
   }
 }
-__device__ __forceinline__ bool warp_swait(uint64_t* bar, uint32_t parity, SBarriers* bars,
+template <class Bars>
+__device__ __forceinline__ bool warp_swait(uint64_t* bar, uint32_t parity, Bars* bars,
                                            uint64_t limit_ns, unsigned int site) {
   return __all_sync(0xffffffffu, swait(bar, parity, bars, limit_ns, site));
 }
@@ -139,6 +146,21 @@ struct SJob {
   int row, group, len, n_kv;
 };
 
+// A position in a ring of n slots (the ring depths are run-time values, so
+// positions advance by one instead of being divided out of a counter).
+struct RingPos {
+  int idx = 0;
+  uint32_t phase = 0;  // completed laps, mod 2: the parity of this slot's current use
+  bool lapped = false;  // some slot has been used before
+  __device__ __forceinline__ void next(int n) {
+    if (++idx == n) {
+      idx = 0;
+      phase ^= 1u;
+      lapped = true;
+    }
+  }
+};
+
 __device__ __forceinline__ bool job_of(const sdpa_impl::SparseParams& p, int j, SJob& job) {
   if (j >= p.total_q * p.n_groups) return false;
   job.row = j / p.n_groups;
@@ -150,7 +172,259 @@ __device__ __forceinline__ bool job_of(const sdpa_impl::SparseParams& p, int j, 
   return true;
 }
 
+// One 128-key tile of a head row's online softmax, in the log2 domain (the
+// calling thread owns the row; s holds its raw scores): keys whose bit in km
+// is clear are removed, the running maximum m_used moves only when the
+// tile's extremum passes it by more than 2^8 (need = true; l is then scaled
+// by the returned alpha), and the exponentials are added to l and packed
+// into P.  With a negative scale the extremum is the minimum (mval = +inf).
+template <bool BF16>
+__device__ __forceinline__ float softmax_tile(float (&s)[kKeys], const uint32_t (&km)[4],
+                                              float sl2, bool pos_scale, float mval,
+                                              float& m_used, float& l, bool& need,
+                                              uint32_t (&pk)[kKeys / 2]) {
+  const bool all_valid = (km[0] & km[1] & km[2] & km[3]) == 0xffffffffu;
+  if (!all_valid) {
+#pragma unroll
+    for (int c = 0; c < kKeys; ++c) s[c] = ((km[c >> 5] >> (c & 31)) & 1u) ? s[c] : mval;
+  }
+  // row extremum: eight independent chains of three-input max / min
+  float e8[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) e8[i] = s[i];
+  if (pos_scale) {
+#pragma unroll
+    for (int c = 8; c < kKeys; c += 16)
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        e8[i] = max3f(e8[i], s[c + i], s[c + 8 + i < kKeys ? c + 8 + i : c + i]);
+    e8[0] = max3f(e8[0], e8[1], e8[2]);
+    e8[3] = max3f(e8[3], e8[4], e8[5]);
+    e8[6] = fmaxf(e8[6], e8[7]);
+    e8[0] = max3f(e8[0], e8[3], e8[6]);
+  } else {
+#pragma unroll
+    for (int c = 8; c < kKeys; c += 16)
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        e8[i] = min3f(e8[i], s[c + i], s[c + 8 + i < kKeys ? c + 8 + i : c + i]);
+    e8[0] = min3f(e8[0], e8[1], e8[2]);
+    e8[3] = min3f(e8[3], e8[4], e8[5]);
+    e8[6] = fminf(e8[6], e8[7]);
+    e8[0] = min3f(e8[0], e8[3], e8[6]);
+  }
+  const float ext = e8[0];
+  const float m_tile = (ext == mval) ? -INFINITY : ext * sl2;
+  need = m_tile > m_used + kRescaleLog2;
+  float alpha = 1.0f;
+  if (need) {
+    alpha = ex2(m_used - m_tile);
+    m_used = m_tile;
+    l *= alpha;
+  }
+  const float neg_m = (m_used == -INFINITY) ? 0.0f : -m_used;
+#pragma unroll
+  for (int c = 0; c < kKeys; c += 2) fma2_bcast(s[c], s[c + 1], s[c], s[c + 1], sl2, neg_m);
+#pragma unroll
+  for (int c = 0; c < kKeys; ++c) s[c] = ex2(s[c]);
+  float rs[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) rs[i] = 0.0f;
+#pragma unroll
+  for (int c = 0; c < kKeys / 2; ++c) {
+    add2_acc(rs[2 * (c & 3)], rs[2 * (c & 3) + 1], s[2 * c], s[2 * c + 1]);
+    pk[c] = pack2<BF16>(s[2 * c], s[2 * c + 1]);
+  }
+  add2_acc(rs[0], rs[1], rs[2], rs[3]);
+  add2_acc(rs[4], rs[5], rs[6], rs[7]);
+  add2_acc(rs[0], rs[1], rs[4], rs[5]);
+  l += rs[0] + rs[1];
+  return alpha;
+}
+
+// Scales the D accumulator columns of the calling thread's TMEM lane
+// (t_o: its lane and first column) by alpha.
+template <int D>
+__device__ __forceinline__ void rescale_row(uint32_t t_o, float alpha) {
+#pragma unroll
+  for (int c = 0; c < D / 32; ++c) {
+    uint32_t o[32];
+    tmem_ld32(t_o + c * 32, o);
+    tmem_ld_wait();
+    float* of = reinterpret_cast<float*>(o);
+#pragma unroll
+    for (int e = 0; e < 32; e += 2) mul2_bcast(of[e], of[e + 1], alpha);
+    tmem_st32(t_o + c * 32, o);
+  }
+}
+
+// Reads the calling thread's accumulator row (t_o as above) and, when
+// `store`, writes it times inv_l as D elements at orow.
 template <int D, bool BF16>
+__device__ __forceinline__ void store_row(uint32_t t_o, float inv_l, uint16_t* orow, bool store) {
+#pragma unroll
+  for (int c = 0; c < D / 32; ++c) {
+    uint32_t o[32];
+    tmem_ld32(t_o + c * 32, o);
+    tmem_ld_wait();
+    uint32_t pw[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e)
+      pw[e] = pack2<BF16>(__uint_as_float(o[2 * e]) * inv_l, __uint_as_float(o[2 * e + 1]) * inv_l);
+    if (store) {
+      uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+      for (int v = 0; v < 4; ++v)
+        dst[v] = make_uint4(pw[4 * v], pw[4 * v + 1], pw[4 * v + 2], pw[4 * v + 3]);
+    }
+  }
+}
+
+// The no-key row: zeros and lse = -inf (the safe softmax of an empty row).
+template <int D>
+__device__ __forceinline__ void store_empty_row(const sdpa_impl::SparseParams& p, int row, int h) {
+  uint16_t* orow = reinterpret_cast<uint16_t*>(p.out) + row * p.o_st + h * p.o_sh;
+  for (int c = 0; c < D; c += 8) *reinterpret_cast<uint4*>(orow + c) = make_uint4(0, 0, 0, 0);
+  if (p.lse != nullptr) p.lse[row * p.lse_st + h * p.lse_sh] = -INFINITY;
+}
+
+// O / l and the log-sum-exp of a finished head row.
+template <int D, bool BF16>
+__device__ __forceinline__ void finish_row(const sdpa_impl::SparseParams& p, uint32_t t_o, int row,
+                                           int h, float m_used, float l) {
+  const float inv_l = (l > 0.0f) ? (1.0f / l) : 0.0f;
+  if (h < p.H && p.lse != nullptr) {
+    constexpr float kLn2 = 0.693147180559945309f;
+    p.lse[row * p.lse_st + h * p.lse_sh] = (l > 0.0f) ? (log2f(l) + m_used) * kLn2 : -INFINITY;
+  }
+  uint16_t* orow = reinterpret_cast<uint16_t*>(p.out) + row * p.o_st + h * p.o_sh;
+  store_row<D, BF16>(t_o, inv_l, orow, h < p.H);
+}
+
+// ---- The half-row form (groups of at most 64 heads).  Head h of the group
+// sits in TMEM lane 32 (h / 16) + h % 16, so each warp of the softmax
+// warpgroup owns 16 rows, and threads t and t + 16 share row t: keys
+// [0, 64) and [64, 128) of every tile, and the first and second halves of
+// the row's accumulator columns.
+
+// One tile's step on a half row (s: its 64 raw scores, km0 / km1: the
+// validity bits of its keys).  The extremum is exchanged with the partner
+// thread, so both take the same rescale decision; l is the half row's sum.
+template <bool BF16>
+__device__ __forceinline__ float softmax_half_tile(float (&s)[kKeys / 2], uint32_t km0,
+                                                   uint32_t km1, float sl2, bool pos_scale,
+                                                   float mval, float& m_used, float& l,
+                                                   bool& need, uint32_t (&pk)[kKeys / 4]) {
+  constexpr int kN = kKeys / 2;
+  if ((km0 & km1) != 0xffffffffu) {
+#pragma unroll
+    for (int c = 0; c < kN; ++c)
+      s[c] = (((c < 32 ? km0 : km1) >> (c & 31)) & 1u) ? s[c] : mval;
+  }
+  float e8[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) e8[i] = s[i];
+  if (pos_scale) {
+#pragma unroll
+    for (int c = 8; c < kN; c += 16)
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        e8[i] = max3f(e8[i], s[c + i], s[c + 8 + i < kN ? c + 8 + i : c + i]);
+    e8[0] = max3f(e8[0], e8[1], e8[2]);
+    e8[3] = max3f(e8[3], e8[4], e8[5]);
+    e8[6] = fmaxf(e8[6], e8[7]);
+    e8[0] = max3f(e8[0], e8[3], e8[6]);
+    e8[0] = fmaxf(e8[0], __shfl_xor_sync(0xffffffffu, e8[0], 16));
+  } else {
+#pragma unroll
+    for (int c = 8; c < kN; c += 16)
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        e8[i] = min3f(e8[i], s[c + i], s[c + 8 + i < kN ? c + 8 + i : c + i]);
+    e8[0] = min3f(e8[0], e8[1], e8[2]);
+    e8[3] = min3f(e8[3], e8[4], e8[5]);
+    e8[6] = fminf(e8[6], e8[7]);
+    e8[0] = min3f(e8[0], e8[3], e8[6]);
+    e8[0] = fminf(e8[0], __shfl_xor_sync(0xffffffffu, e8[0], 16));
+  }
+  const float ext = e8[0];
+  const float m_tile = (ext == mval) ? -INFINITY : ext * sl2;
+  need = m_tile > m_used + kRescaleLog2;
+  float alpha = 1.0f;
+  if (need) {
+    alpha = ex2(m_used - m_tile);
+    m_used = m_tile;
+    l *= alpha;
+  }
+  const float neg_m = (m_used == -INFINITY) ? 0.0f : -m_used;
+#pragma unroll
+  for (int c = 0; c < kN; c += 2) fma2_bcast(s[c], s[c + 1], s[c], s[c + 1], sl2, neg_m);
+#pragma unroll
+  for (int c = 0; c < kN; ++c) s[c] = ex2(s[c]);
+  float rs[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) rs[i] = 0.0f;
+#pragma unroll
+  for (int c = 0; c < kN / 2; ++c) {
+    add2_acc(rs[2 * (c & 3)], rs[2 * (c & 3) + 1], s[2 * c], s[2 * c + 1]);
+    pk[c] = pack2<BF16>(s[2 * c], s[2 * c + 1]);
+  }
+  add2_acc(rs[0], rs[1], rs[2], rs[3]);
+  add2_acc(rs[4], rs[5], rs[6], rs[7]);
+  add2_acc(rs[0], rs[1], rs[4], rs[5]);
+  l += rs[0] + rs[1];
+  return alpha;
+}
+
+// Scales the calling thread's half of its row's D accumulator columns (t_o:
+// the warp's lane base and the first column).
+template <int D>
+__device__ __forceinline__ void rescale_half_row(uint32_t t_o, float alpha) {
+#pragma unroll
+  for (int c = 0; c < D / 64; ++c) {
+    uint32_t o[32];
+    tmem_ld16x2_32<D / 2>(t_o + c * 32, o);
+    tmem_ld_wait();
+    float* of = reinterpret_cast<float*>(o);
+#pragma unroll
+    for (int e = 0; e < 32; e += 2) mul2_bcast(of[e], of[e + 1], alpha);
+    tmem_st16x2_32<D / 2>(t_o + c * 32, o);
+  }
+}
+
+// O / l (l: the half row's sum, added to its partner's here) and the
+// log-sum-exp of a finished row; each thread writes its half of the D
+// elements.
+template <int D, bool BF16>
+__device__ __forceinline__ void finish_half_row(const sdpa_impl::SparseParams& p, uint32_t t_o,
+                                                int row, int h, int half, float m_used,
+                                                float l_part) {
+  const float l = l_part + __shfl_xor_sync(0xffffffffu, l_part, 16);
+  const float inv_l = (l > 0.0f) ? (1.0f / l) : 0.0f;
+  if (h < p.H && half == 0 && p.lse != nullptr) {
+    constexpr float kLn2 = 0.693147180559945309f;
+    p.lse[row * p.lse_st + h * p.lse_sh] = (l > 0.0f) ? (log2f(l) + m_used) * kLn2 : -INFINITY;
+  }
+  uint16_t* orow = reinterpret_cast<uint16_t*>(p.out) + row * p.o_st + h * p.o_sh + half * (D / 2);
+#pragma unroll
+  for (int c = 0; c < D / 64; ++c) {
+    uint32_t o[32];
+    tmem_ld16x2_32<D / 2>(t_o + c * 32, o);
+    tmem_ld_wait();
+    uint32_t pw[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e)
+      pw[e] = pack2<BF16>(__uint_as_float(o[2 * e]) * inv_l, __uint_as_float(o[2 * e + 1]) * inv_l);
+    if (h < p.H) {
+      uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+      for (int v = 0; v < 4; ++v)
+        dst[v] = make_uint4(pw[4 * v], pw[4 * v + 1], pw[4 * v + 2], pw[4 * v + 3]);
+    }
+  }
+}
+
+template <int D, bool BF16, bool HALF>
 __global__ void __launch_bounds__(kThreads, 1)
     sparse_fwd_kernel(const __grid_constant__ sdpa_impl::SparseParams p) {
   using Lay = SLayout<D>;
@@ -175,7 +449,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->q_empty, 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(&bars->s_full[b], 1);
-      mbar_init(&bars->s_free[b], kRows / 32);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&bars->p_ready[b], kRows / 32);
@@ -185,13 +458,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->fin, 1);
     for (int s = 0; s < kMaxStages + 2; ++s) mbar_init(&bars->m_full[s], kGatherWarps);
     for (int s = 0; s < kMaxStages; ++s) {
-      mbar_init(&bars->k_full[s], kGatherWarps);
+      mbar_init(&bars->k_full[s], kGatherWarps * 32);  // one arrival per gathering thread
       mbar_init(&bars->k_empty[s], 1);
-      mbar_init(&bars->v_full[s], kGatherWarps);
       mbar_init(&bars->v_empty[s], 1);
     }
     bars->abort_flag = 0;
     fence_barrier_init();
+  }
+  if (HALF) {
+    // rows of the Q tile that hold no head are never loaded: zero them once,
+    // so the products read finite values there
+    for (int i = threadIdx.x; i < Lay::kTileBytes / 16; i += kThreads)
+      reinterpret_cast<uint4*>(sQ)[i] = make_uint4(0, 0, 0, 0);
+    fence_proxy_async_smem();
   }
   if (warp == 0 && lane == 0) prefetch_tensormap(&p.tm_q);
   if (warp == 1) {
@@ -209,29 +488,37 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------- softmax warps
     regs_increase<kRegsSoftmax>();
     const int wq = warp & 3;
-    const int r = wq * 32 + lane;  // head row within the group
+    // head row within the group, and (half-row form) which half of it
+    const int half = HALF ? (lane >> 4) : 0;
+    const int r = HALF ? wq * 16 + (lane & 15) : wq * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
     const float sl2 = p.scale_log2;
     const bool pos_scale = sl2 >= 0.0f;
     const float mval = pos_scale ? -INFINITY : INFINITY;
     uint32_t ns = 0;
-    int g = 0;  // K tile counter (mask slot)
+    RingPos mslot;  // key-mask slot of the next tile
     bool ok = true;
     SJob job;
     for (int jj = static_cast<int>(blockIdx.x); ok && job_of(p, jj, job); jj += step) {
       const int h = job.group * kRows + r;
       if (job.n_kv == 0) {
         // no key: zeros and lse = -inf (the safe softmax of an empty row)
-        if (h < p.H) {
-          uint16_t* orow = reinterpret_cast<uint16_t*>(p.out) + job.row * p.o_st + h * p.o_sh;
-          for (int c = 0; c < D; c += 8)
-            *reinterpret_cast<uint4*>(orow + c) = make_uint4(0, 0, 0, 0);
-          if (p.lse != nullptr) p.lse[job.row * p.lse_st + h * p.lse_sh] = -INFINITY;
+        if (HALF) {
+          if (h < p.H) {
+            uint16_t* orow = reinterpret_cast<uint16_t*>(p.out) + job.row * p.o_st + h * p.o_sh +
+                             half * (D / 2);
+            for (int c = 0; c < D / 2; c += 8)
+              *reinterpret_cast<uint4*>(orow + c) = make_uint4(0, 0, 0, 0);
+            if (half == 0 && p.lse != nullptr)
+              p.lse[job.row * p.lse_st + h * p.lse_sh] = -INFINITY;
+          }
+        } else if (h < p.H) {
+          store_empty_row<D>(p, job.row, h);
         }
         continue;
       }
       float m_used = -INFINITY, l = 0.0f;
-      for (int j = 0; j < job.n_kv; ++j, ++g) {
+      for (int j = 0; j < job.n_kv; ++j) {
         const uint32_t b = ns & 1;
         if (!warp_swait(&bars->s_full[b], (ns >> 1) & 1, bars, limit, kSpS)) {
           ok = false;
@@ -239,91 +526,44 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ++ns;
         tc_fence_after();
-        float s[kKeys];
+        constexpr int kPer = HALF ? kKeys / 2 : kKeys;  // scores per thread
+        float s[kPer];
         {
-          uint32_t su[kKeys];
+          uint32_t su[kPer];
 #pragma unroll
-          for (int c = 0; c < kKeys / 32; ++c)
-            tmem_ld32(tmem + kColS0 + b * 128 + lane_off + c * 32, su + c * 32);
+          for (int c = 0; c < kPer / 32; ++c) {
+            if (HALF)
+              tmem_ld16x2_32<kKeys / 2>(tmem + kColS0 + b * 128 + lane_off + c * 32, su + c * 32);
+            else
+              tmem_ld32(tmem + kColS0 + b * 128 + lane_off + c * 32, su + c * 32);
+          }
           tmem_ld_wait();
 #pragma unroll
-          for (int c = 0; c < kKeys; ++c) s[c] = __uint_as_float(su[c]);
+          for (int c = 0; c < kPer; ++c) s[c] = __uint_as_float(su[c]);
         }
-        // The key mask is read before S's buffer is released: the producer
-        // refills this slot only after S of a tile two later has completed,
-        // which needs that release (mask slots = stages + 2), so m_full of
-        // the slot is at most one phase ahead of this wait.
+        // The gathers refill this mask slot (mask slots = stages + 2) only
+        // once the stage of the tile two after this one is free again, which
+        // needs that tile's P and so this tile's: m_full of the slot is at
+        // most one phase ahead of this wait.
         uint32_t km[4];
-        if (!warp_swait(&bars->m_full[g % n_slots], (g / n_slots) & 1, bars, limit,
-                        kSpK)) {
+        if (!warp_swait(&bars->m_full[mslot.idx], mslot.phase, bars, limit, kSpK)) {
           ok = false;
           break;
         }
         {
-          const volatile uint32_t* src = bars->kmask[g % n_slots];
+          const volatile uint32_t* src = bars->kmask[mslot.idx];
 #pragma unroll
           for (int e = 0; e < 4; ++e) km[e] = src[e];
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->s_free[b]);
-        const bool all_valid = (km[0] & km[1] & km[2] & km[3]) == 0xffffffffu;
-        if (!all_valid) {
-#pragma unroll
-          for (int c = 0; c < kKeys; ++c) s[c] = ((km[c >> 5] >> (c & 31)) & 1u) ? s[c] : mval;
-        }
-        // row extremum: eight independent chains of three-input max / min
-        float e8[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) e8[i] = s[i];
-        if (pos_scale) {
-#pragma unroll
-          for (int c = 8; c < kKeys; c += 16)
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-              e8[i] = max3f(e8[i], s[c + i], s[c + 8 + i < kKeys ? c + 8 + i : c + i]);
-          e8[0] = max3f(e8[0], e8[1], e8[2]);
-          e8[3] = max3f(e8[3], e8[4], e8[5]);
-          e8[6] = fmaxf(e8[6], e8[7]);
-          e8[0] = max3f(e8[0], e8[3], e8[6]);
-        } else {
-#pragma unroll
-          for (int c = 8; c < kKeys; c += 16)
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-              e8[i] = min3f(e8[i], s[c + i], s[c + 8 + i < kKeys ? c + 8 + i : c + i]);
-          e8[0] = min3f(e8[0], e8[1], e8[2]);
-          e8[3] = min3f(e8[3], e8[4], e8[5]);
-          e8[6] = fminf(e8[6], e8[7]);
-          e8[0] = min3f(e8[0], e8[3], e8[6]);
-        }
-        const float ext = e8[0];
-        const float m_tile = (ext == mval) ? -INFINITY : ext * sl2;
-        const bool need = m_tile > m_used + kRescaleLog2;
-        float alpha = 1.0f;
-        if (need) {
-          alpha = ex2(m_used - m_tile);
-          m_used = m_tile;
-          l *= alpha;
-        }
-        const float neg_m = (m_used == -INFINITY) ? 0.0f : -m_used;
-#pragma unroll
-        for (int c = 0; c < kKeys; c += 2) fma2_bcast(s[c], s[c + 1], s[c], s[c + 1], sl2, neg_m);
-#pragma unroll
-        for (int c = 0; c < kKeys; ++c) s[c] = ex2(s[c]);
-        uint32_t pk[kKeys / 2];
-        float rs[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) rs[i] = 0.0f;
-#pragma unroll
-        for (int c = 0; c < kKeys / 2; ++c) {
-          add2_acc(rs[2 * (c & 3)], rs[2 * (c & 3) + 1], s[2 * c], s[2 * c + 1]);
-          pk[c] = pack2<BF16>(s[2 * c], s[2 * c + 1]);
-        }
-        add2_acc(rs[0], rs[1], rs[2], rs[3]);
-        add2_acc(rs[4], rs[5], rs[6], rs[7]);
-        add2_acc(rs[0], rs[1], rs[4], rs[5]);
-        l += rs[0] + rs[1];
+        mslot.next(n_slots);
+        bool need;
+        uint32_t pk[kPer / 2];
+        float alpha;
+        if constexpr (HALF)
+          alpha = softmax_half_tile<BF16>(s, half ? km[2] : km[0], half ? km[3] : km[1], sl2,
+                                          pos_scale, mval, m_used, l, need, pk);
+        else
+          alpha = softmax_tile<BF16>(s, km, sl2, pos_scale, mval, m_used, l, need, pk);
         // Global tile index t (all jobs of this CTA).  Each wait below is
         // on a barrier whose next phase needs this tile's P, so it can never
         // fall two phases behind.
@@ -335,18 +575,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          {
-#pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-              uint32_t o[32];
-              tmem_ld32(tmem + kColO + lane_off + c * 32, o);
-              tmem_ld_wait();
-              float* of = reinterpret_cast<float*>(o);
-#pragma unroll
-              for (int e = 0; e < 32; e += 2) mul2_bcast(of[e], of[e + 1], alpha);
-              tmem_st32(tmem + kColO + lane_off + c * 32, o);
-            }
-          }
+          if (HALF)
+            rescale_half_row<D>(tmem + kColO + lane_off, alpha);
+          else
+            rescale_row<D>(tmem + kColO + lane_off, alpha);
         }
         // P buffer t & 1 is free once PV(t-2) is done.
         const uint32_t pb = t & 1;
@@ -357,8 +589,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_after();
         }
-        tmem_st32(tmem + kColP + pb * 64 + lane_off, pk);
-        tmem_st32(tmem + kColP + pb * 64 + lane_off + 32, pk + 32);
+        if constexpr (HALF) {
+          tmem_st16x2_32<kKeys / 4>(tmem + kColP + pb * 64 + lane_off, pk);
+        } else {
+          tmem_st32(tmem + kColP + pb * 64 + lane_off, pk);
+          tmem_st32(tmem + kColP + pb * 64 + lane_off + 32, pk + 32);
+        }
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
@@ -371,30 +607,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after();
-      const float inv_l = (l > 0.0f) ? (1.0f / l) : 0.0f;
-      if (h < p.H && p.lse != nullptr) {
-        constexpr float kLn2 = 0.693147180559945309f;
-        p.lse[job.row * p.lse_st + h * p.lse_sh] = (l > 0.0f) ? (log2f(l) + m_used) * kLn2
-                                                              : -INFINITY;
-      }
-      uint16_t* orow = reinterpret_cast<uint16_t*>(p.out) + job.row * p.o_st + h * p.o_sh;
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t o[32];
-        tmem_ld32(tmem + kColO + lane_off + c * 32, o);
-        tmem_ld_wait();
-        uint32_t pw[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e)
-          pw[e] = pack2<BF16>(__uint_as_float(o[2 * e]) * inv_l,
-                              __uint_as_float(o[2 * e + 1]) * inv_l);
-        if (h < p.H) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
-#pragma unroll
-          for (int v = 0; v < 4; ++v)
-            dst[v] = make_uint4(pw[4 * v], pw[4 * v + 1], pw[4 * v + 2], pw[4 * v + 3]);
-        }
-      }
+      if (HALF)
+        finish_half_row<D, BF16>(p, tmem + kColO + lane_off, job.row, h, half, m_used, l);
+      else
+        finish_row<D, BF16>(p, tmem + kColO + lane_off, job.row, h, m_used, l);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->o_free);
@@ -411,11 +627,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (job.n_kv == 0) continue;
       if (jobs > 0 && !warp_swait(&bars->q_empty, (jobs - 1) & 1, bars, limit, kSpEmpty)) break;
       if (leader) {
-        mbar_arrive_expect_tx(&bars->q_full, Lay::kChunks * p.q_rows * 128);
+        if (HALF) {
+          // heads 16 i .. 16 i + 15 into rows 32 i .. 32 i + 15
+          const int box = min(16, p.H), n_box = (p.H + 15) / 16;
+          mbar_arrive_expect_tx(&bars->q_full, Lay::kChunks * n_box * box * 128);
 #pragma unroll
-        for (int c = 0; c < Lay::kChunks; ++c)
-          tma_load_3d(sQ + c * Lay::kChunkBytes, &p.tm_q, &bars->q_full, c * 64,
-                      job.group * kRows, job.row);
+          for (int c = 0; c < Lay::kChunks; ++c)
+            for (int i = 0; i < n_box; ++i)
+              tma_load_3d(sQ + c * Lay::kChunkBytes + i * 32 * 128, &p.tm_q, &bars->q_full,
+                          c * 64, i * 16, job.row);
+        } else {
+          mbar_arrive_expect_tx(&bars->q_full, Lay::kChunks * p.q_rows * 128);
+#pragma unroll
+          for (int c = 0; c < Lay::kChunks; ++c)
+            tma_load_3d(sQ + c * Lay::kChunkBytes, &p.tm_q, &bars->q_full, c * 64,
+                        job.group * kRows, job.row);
+        }
       }
       ++jobs;
     }
@@ -425,36 +652,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Warp w (8..11) copies key rows 32(w-8) .. +31 of every tile, 16 bytes
     // per cp.async, into the 128-byte-swizzled K-major layout the products
     // read (piece q of a 128-byte row r lands at q ^ (r & 7)); lane l loads
-    // the index of row +l, and the copies are spread so that one warp
-    // instruction moves whole contiguous rows (D/8 lanes per row).  A tile
-    // is signalled once its copies are done, `lag` tiles behind the newest,
-    // so later tiles' copies are in flight meanwhile; each thread fences its
-    // completed copies for the tensor core's proxy before the warp arrives.
+    // the index of row +l, and four lanes share each row (see copy_rows), so
+    // one warp instruction moves 64 contiguous bytes of each of 8 rows.  Each
+    // thread then arrives on the stage's k_full through the copy unit, which
+    // fires once that thread's copies have landed: a tile is announced as
+    // soon as it is in shared memory, and the gathers never wait for their
+    // own copies (the issuing warp fences them for the tensor core's proxy
+    // after its wait).
     const int wrow = (warp - 8) * 32;
     const uint8_t* kbase = reinterpret_cast<const uint8_t*>(p.k);
     const uint8_t* vbase = reinterpret_cast<const uint8_t*>(p.v);
     constexpr int kPieces = D / 8;          // 16-byte pieces per row
-    constexpr int kRowsPerOp = 32 / kPieces;
-    const int piece = lane % kPieces;
-    const int pc_chunk = piece >> 3, pc_q = piece & 7;
-    int g = 0, signalled = 0;
-    // Copies in flight per warp: fewer than the ring's free stages (the MMA
-    // holds two), and on the shared-kv ring two rather than four -- a tile
-    // is announced sooner after its copies land, which the products wait
-    // for (measured: 486 vs 464 TFLOP/s on the top-2048 workload; one is
-    // slower again).
-    const int lag = max(1, min(nst - 4, 4));
+    RingPos stage, mslot;  // ring stage and key-mask slot of the next tile
     bool ok = true;
-    auto signal_oldest = [&]() {
-      const int s = signalled % nst;
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&bars->k_full[s]);
-        mbar_arrive(&bars->v_full[s]);
-      }
-      ++signalled;
-    };
     SJob job;
     for (int jj = static_cast<int>(blockIdx.x); ok && job_of(p, jj, job); jj += step) {
       if (job.n_kv == 0) continue;
@@ -464,66 +674,59 @@ __global__ void __launch_bounds__(kThreads, 1)
         return (ta < job.len) ? __ldg(irow + ta) : -1;
       };
       int na = load_idx(0);
-      for (int j = 0; j < job.n_kv; ++j, ++g) {
-        const int s = g % nst;
-        const int use = g / nst;
+      for (int j = 0; j < job.n_kv; ++j) {
+        const int s = stage.idx;
         // an entry past the row's count or outside [0, total_k) reads row 0
         // and is removed by the softmax through the mask
         const bool va = na >= 0 && na < p.total_k;
         const int ra = va ? na : 0;
         const uint32_t ba = __ballot_sync(0xffffffffu, va);
         if (j + 1 < job.n_kv) na = load_idx(j + 1);
-        if (use > 0) {
-          const uint32_t par = (use - 1) & 1;
-          const bool free_now = __all_sync(
-              0xffffffffu, mbar_test_wait(&bars->k_empty[s], par) &&
-                               (p.kv_shared || mbar_test_wait(&bars->v_empty[s], par)));
-          if (!free_now) {
-            // About to block on a stage: first finish and signal every tile
-            // still in flight, so the consumers never wait on copies that are
-            // done but not yet announced.
-            cp_async_wait<0>();
-            while (signalled < g) signal_oldest();
-            if (!warp_swait(&bars->k_empty[s], par, bars, limit, kSpEmpty) ||
-                (!p.kv_shared && !warp_swait(&bars->v_empty[s], par, bars, limit, kSpEmpty))) {
-              ok = false;
-              break;
-            }
+        if (stage.lapped) {
+          // the stage's previous use, one lap ago
+          const uint32_t par = stage.phase ^ 1u;
+          if (!warp_swait(&bars->k_empty[s], par, bars, limit, kSpEmpty) ||
+              (!p.kv_shared && !warp_swait(&bars->v_empty[s], par, bars, limit, kSpEmpty))) {
+            ok = false;
+            break;
           }
         }
         if (lane == 0) {
-          volatile uint32_t* dst = bars->kmask[g % n_slots];
+          volatile uint32_t* dst = bars->kmask[mslot.idx];
           dst[warp - 8] = ba;  // keys wrow .. +31
-          mbar_arrive(&bars->m_full[g % n_slots]);  // release: the mask is written
+          mbar_arrive(&bars->m_full[mslot.idx]);  // release: the mask is written
         }
+        mslot.next(n_slots);
+        // Four lanes a row: lane l copies pieces c, c + 4, ... (c = l % 4) of
+        // rows l / 4 + 8 i (i < 4), so one instruction moves 64 contiguous
+        // bytes of each of 8 rows, the swizzle term (row & 7) = l / 4 is the
+        // lane's own, and the lane needs four row indices a tile.
+        int64_t roff[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          roff[i] = static_cast<int64_t>(__shfl_sync(0xffffffffu, ra, (lane >> 2) + 8 * i));
         auto copy_rows = [&](const uint8_t* base, int64_t row_bytes, uint8_t* stage) {
-#pragma unroll 4
-          for (int k = 0; k < 32 / kRowsPerOp; ++k) {
-            const int m = k * kRowsPerOp + lane / kPieces;  // row within this warp's 32
-            const int ridx = __shfl_sync(0xffffffffu, ra, m);
-            const int r = wrow + m;
-            cp_async_16(stage + pc_chunk * Lay::kChunkBytes + r * 128 + ((pc_q ^ (r & 7)) << 4),
-                        base + static_cast<int64_t>(ridx) * row_bytes + piece * 16);
+          const int c4 = lane & 3, r8 = lane >> 2;
+          uint8_t* sdst = stage + (wrow + r8) * 128;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const uint8_t* gsrc = base + roff[i] * row_bytes + c4 * 16;
+#pragma unroll
+            for (int pp = 0; pp < kPieces / 4; ++pp) {
+              const int q = 4 * pp + c4;  // piece of the row
+              cp_async_16(sdst + i * 1024 + (q >> 3) * Lay::kChunkBytes + (((q & 7) ^ r8) << 4),
+                          gsrc + pp * 64);
+            }
           }
         };
         copy_rows(kbase, p.k_row_bytes, sK + s * Lay::kTileBytes);
         if (!p.kv_shared) copy_rows(vbase, p.v_row_bytes, sV + s * Lay::kTileBytes);
         cp_async_commit();
-        // Keep `lag` tiles of copies in flight (fewer than the ring depth,
-        // so the next tile's stage is always one that was signalled).
-        if (g + 1 - signalled > lag) {
-          switch (lag) {
-            case 1: cp_async_wait<1>(); break;
-            case 2: cp_async_wait<2>(); break;
-            case 3: cp_async_wait<3>(); break;
-            default: cp_async_wait<4>(); break;
-          }
-          while (g + 1 - signalled > lag) signal_oldest();
-        }
+        cp_async_mbar_arrive_noinc(&bars->k_full[s]);
+        stage.next(nst);
       }
     }
     cp_async_wait<0>();
-    while (signalled < g) signal_oldest();
   } else if (warp == 1) {
     // ------------------------------------------------------ MMA issue
     constexpr uint32_t idS = idesc_f16_f32acc(BF16, false, kRows, kKeys);
@@ -534,62 +737,68 @@ __global__ void __launch_bounds__(kThreads, 1)
     // V rows: their own stages, or the K stage when one kv tensor serves both
     const uint32_t v_lo = desc_lo_sw128(smem_addr(p.kv_shared ? sK : sV), Lay::kChunkBytes);
     bool issued_any = false;
+    // Four K-steps per elected issue: S over each 64-column chunk of D (32
+    // bytes a step in both operands), PV over each 64-key half of the tile
+    // (8 TMEM columns of P and 16 V rows a step).
     auto issue_s = [&](uint32_t buf, int s) {
       const uint32_t b0 = k_lo + static_cast<uint32_t>(s * (Lay::kTileBytes >> 4));
 #pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t off = ((kk >> 2) * Lay::kChunkBytes + (kk & 3) * 32) >> 4;
-        mma_ss_elect<kHi, kHi>(tmem + kColS0 + buf * 128, q_lo + off, b0 + off, idS,
-                               kk > 0 ? 1u : 0u);
+      for (int c = 0; c < Lay::kChunks; ++c) {
+        const uint32_t off = static_cast<uint32_t>(c * Lay::kChunkBytes) >> 4;
+        mma_ss_x4<kHi, kHi>(tmem + kColS0 + buf * 128, q_lo + off, b0 + off, 2u, 2u, idS,
+                            c > 0 ? 1u : 0u);
       }
       mma_commit_elect(&bars->s_full[buf]);
     };
     auto issue_pv = [&](int s, uint32_t pb, bool accumulate) {
       const uint32_t b0 = v_lo + static_cast<uint32_t>(s * (Lay::kTileBytes >> 4));
 #pragma unroll
-      for (int kk = 0; kk < kKeys / 16; ++kk)
-        mma_ts_elect<kHi>(tmem + kColO, tmem + kColP + pb * 64 + kk * 8,
-                          b0 + ((kk * 16 * 128) >> 4), idPV, (accumulate || kk > 0) ? 1u : 0u);
+      for (int h = 0; h < 2; ++h)
+        mma_ts_x4<kHi>(tmem + kColO, tmem + kColP + pb * 64 + h * 32, b0 + h * ((64 * 128) >> 4),
+                       8u, (16 * 128) >> 4, idPV, (accumulate || h > 0) ? 1u : 0u);
       mma_commit_elect(&bars->o_done[pb]);
     };
     int g = 0, jobs = 0;
     uint32_t ns = 0;
+    RingPos s_pos, pv_pos;  // ring stages of the next S and the next PV
     bool ok = true;
     SJob job;
-    // S into the buffer of S(ns); its previous contents (S(ns-2)) must be in
-    // the softmax's registers.
-    auto s_next = [&](int s) -> bool {
-      const uint32_t buf = ns & 1;
-      if (ns >= 2 && !warp_swait(&bars->s_free[buf], ((ns >> 1) - 1) & 1, bars, limit, kSpSFree))
-        return false;
+    // S into the buffer of S(ns).  Its previous contents, S(ns-2), are in
+    // the softmax's registers: the loop below waited for P(ns-2), stored
+    // after that load, before issuing PV(ns-2), which precedes this issue.
+    auto s_next = [&](int s) {
+      // the stage's rows were written by the gathers' copies (generic proxy)
+      // and are read by the tensor core (async proxy): the k_full wait
+      // acquired them, this fence orders them before the products
+      fence_proxy_async_smem();
       tc_fence_after();
-      issue_s(buf, s);
+      issue_s(ns & 1, s);
       if (!p.kv_shared) mma_commit_elect(&bars->k_empty[s]);  // else after PV
       ++ns;
-      return true;
     };
     for (int jj = static_cast<int>(blockIdx.x); ok && job_of(p, jj, job); jj += step) {
       if (job.n_kv == 0) continue;
       if (!warp_swait(&bars->q_full, jobs & 1, bars, limit, kSpQ) ||
-          !warp_swait(&bars->k_full[g % nst], (g / nst) & 1, bars, limit, kSpK) ||
-          !s_next(g % nst))
+          !warp_swait(&bars->k_full[s_pos.idx], s_pos.phase, bars, limit, kSpK))
         break;
+      s_next(s_pos.idx);
+      s_pos.next(nst);
       issued_any = true;
       if (job.n_kv == 1) mma_commit_elect(&bars->q_empty);
       for (int j = 0; j < job.n_kv; ++j) {
         const int gj = g + j;
         if (j + 1 < job.n_kv) {
-          const int s1 = (gj + 1) % nst;
-          if (!warp_swait(&bars->k_full[s1], ((gj + 1) / nst) & 1, bars, limit, kSpK) ||
-              !s_next(s1)) {
+          if (!warp_swait(&bars->k_full[s_pos.idx], s_pos.phase, bars, limit, kSpK)) {
             ok = false;
             break;
           }
+          s_next(s_pos.idx);
+          s_pos.next(nst);
           if (j + 2 == job.n_kv) mma_commit_elect(&bars->q_empty);
         }
-        const int s = gj % nst;
-        if (!warp_swait(&bars->v_full[s], (gj / nst) & 1, bars, limit, kSpV) ||
-            !warp_swait(&bars->p_ready[gj & 1], (gj >> 1) & 1, bars, limit, kSpP)) {
+        // (V of this stage arrived with its K, waited for before its S)
+        const int s = pv_pos.idx;
+        if (!warp_swait(&bars->p_ready[gj & 1], (gj >> 1) & 1, bars, limit, kSpP)) {
           ok = false;
           break;
         }
@@ -603,6 +812,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         issue_pv(s, static_cast<uint32_t>(gj) & 1, j > 0);
         mma_commit_elect(p.kv_shared ? &bars->k_empty[s] : &bars->v_empty[s]);
+        pv_pos.next(nst);
       }
       g += job.n_kv;
       ++jobs;
@@ -654,10 +864,10 @@ __global__ void __launch_bounds__(256) compact_kernel(const sdpa_impl::CompactPa
   if (lane == 0) p.length[row] = n;
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool HALF>
 cudaError_t launch_sparse_one(const sdpa_impl::SparseParams& p, int max_ctas,
                               cudaStream_t stream) {
-  auto kern = sparse_fwd_kernel<D, BF16>;
+  auto kern = sparse_fwd_kernel<D, BF16, HALF>;
   constexpr int smem = SLayout<D>::kTotal;
   static bool configured = false;
   if (!configured) {
@@ -693,11 +903,19 @@ namespace sdpa_impl {
 cudaError_t launch_sparse(const SparseParams& p, int head_dim, bool bf16, int max_ctas,
                           cudaStream_t stream) {
   if (max_ctas < 1) return cudaErrorInvalidValue;
-  if (head_dim == 64)
-    return bf16 ? launch_sparse_one<64, true>(p, max_ctas, stream)
-                : launch_sparse_one<64, false>(p, max_ctas, stream);
-  return bf16 ? launch_sparse_one<128, true>(p, max_ctas, stream)
-              : launch_sparse_one<128, false>(p, max_ctas, stream);
+  const bool half = p.q_half != 0;
+  if (head_dim == 64) {
+    if (half)
+      return bf16 ? launch_sparse_one<64, true, true>(p, max_ctas, stream)
+                  : launch_sparse_one<64, false, true>(p, max_ctas, stream);
+    return bf16 ? launch_sparse_one<64, true, false>(p, max_ctas, stream)
+                : launch_sparse_one<64, false, false>(p, max_ctas, stream);
+  }
+  if (half)
+    return bf16 ? launch_sparse_one<128, true, true>(p, max_ctas, stream)
+                : launch_sparse_one<128, false, true>(p, max_ctas, stream);
+  return bf16 ? launch_sparse_one<128, true, false>(p, max_ctas, stream)
+              : launch_sparse_one<128, false, false>(p, max_ctas, stream);
 }
 
 cudaError_t launch_compact(const CompactParams& p, cudaStream_t stream) {

@@ -149,3 +149,61 @@ def test_one_kv_tensor_for_keys_and_values(sdpa_lib):
                                         torch.from_numpy(idx).to(dev),
                                         torch.from_numpy(length).to(dev))
     assert torch.equal(out, out2)
+
+
+HALF_ROW_CASES = [  # total_q, total_k, H, D, topk, dtype -- groups of at most 64 heads
+    (1, 500, 64, 128, 300, torch.bfloat16),    # one row
+    (7, 800, 48, 128, 200, torch.float16),     # three 16-head boxes
+    (9, 700, 20, 128, 150, torch.bfloat16),    # the second box runs past the heads
+    (5, 300, 8, 64, 100, torch.float16),       # fewer heads than one box
+    (29, 1200, 32, 64, 640, torch.bfloat16),   # head size 64, ragged last tiles
+]
+
+
+@pytest.mark.parametrize("case", HALF_ROW_CASES,
+                         ids=[f"q{c[0]}-k{c[1]}-H{c[2]}-D{c[3]}-topk{c[4]}" for c in HALF_ROW_CASES])
+def test_half_row_form_matches_oracle(sdpa_lib, case):
+    """Groups of at most 64 heads put 16 heads in each quarter of the tile and
+    split every row's keys between two softmax threads."""
+    total_q, total_k, H, D, topk, dtype = case
+    q, k, v, idx, length = make(*case, seed=1400 + H + D + total_q)
+    dev = torch.device("cuda")
+    out, lse = sdpa_lib.sdpa_sparse_forward(
+        q.to(dev), k.to(dev), v.to(dev), torch.from_numpy(idx).to(dev),
+        torch.from_numpy(length).to(dev), return_lse=True)
+    rc, detail = sdpa_lib.sdpa_last_device_status()
+    assert rc == 0, f"device status bits {detail:#x}"
+    ref, ref_lse = oracle.sdpa_sparse(q, k, v, idx, topk_length=length, return_lse=True)
+    check(out.double().cpu().numpy(), ref, "out")
+    got_lse = lse.double().cpu().numpy()
+    fin = np.isfinite(ref_lse)
+    assert np.array_equal(np.isfinite(got_lse), fin)
+    np.testing.assert_allclose(got_lse[fin], ref_lse[fin], rtol=0, atol=2e-3)
+    if total_q > 2:
+        assert np.all(out.cpu()[2].float().numpy() == 0.0)   # the row with no key
+
+
+def test_rows_do_not_depend_on_their_schedule(sdpa_lib):
+    """Dropping the first query row hands every other row to another CTA and
+    position in its job list: each row's output must stay bit-identical."""
+    q, kv, _, idx, length = make(41, 1500, 64, 128, 700, torch.bfloat16, seed=1410)
+    dev = torch.device("cuda")
+    qd, kvd = q.to(dev), kv.to(dev)
+    idd, lnd = torch.from_numpy(idx).to(dev), torch.from_numpy(length).to(dev)
+    full = sdpa_lib.sdpa_sparse_forward(qd, kvd, kvd, idd, lnd)
+    tail = sdpa_lib.sdpa_sparse_forward(qd[1:].contiguous(), kvd, kvd, idd[1:].contiguous(),
+                                        lnd[1:].contiguous())
+    assert sdpa_lib.sdpa_last_device_status()[0] == 0
+    assert torch.equal(full[1:], tail)
+
+
+def test_negative_scale(sdpa_lib):
+    """A negative scale makes the row minimum the stabiliser."""
+    q, k, v, idx, length = make(12, 600, 64, 128, 256, torch.bfloat16, seed=1420)
+    dev = torch.device("cuda")
+    out = sdpa_lib.sdpa_sparse_forward(q.to(dev), k.to(dev), v.to(dev),
+                                       torch.from_numpy(idx).to(dev),
+                                       torch.from_numpy(length).to(dev), scale=-0.2)
+    assert sdpa_lib.sdpa_last_device_status()[0] == 0
+    check(out.double().cpu().numpy(),
+          oracle.sdpa_sparse(q, k, v, idx, topk_length=length, scale=-0.2), "negative scale")
