@@ -575,20 +575,18 @@ sdpa_status sdpa_sparse_forward(const void* q, const void* k, const void* v, voi
   sdpa_impl::SparseParams p;
   std::memset(&p, 0, sizeof(p));
   {
-    // Q: (D, H, total_q); box 64 x up to 128 heads x 1 row (heads past H read as 0)
+    // Q: (D, H, total_q); box 64 x 128 heads x 1 row (heads past H read as 0)
     const cuuint64_t gdim[3] = {static_cast<cuuint64_t>(head_dim),
                                 static_cast<cuuint64_t>(n_heads),
                                 static_cast<cuuint64_t>(total_q)};
     const cuuint64_t gst[2] = {static_cast<cuuint64_t>(sq_h) * 2u,
                                static_cast<cuuint64_t>(total_q > 1 ? sq_t : sq_h * n_heads) * 2u};
     // With fewer than 128 heads the box is H rows (the tile's other rows
-    // are never stored); with at most 64, 16-row boxes placed in the first
-    // half of each 32-row quarter of the tile, so that two softmax threads
-    // share each row instead of half the threads working on padding rows.
+    // are never stored).  With at most 64, the kernel runs its half-row form
+    // (M = 64 products, two softmax threads a row).
     p.q_rows = static_cast<int>(n_heads < 128 ? n_heads : 128);
     p.q_half = (n_heads <= 64) ? 1 : 0;
-    const int box_rows = p.q_half ? (n_heads < 16 ? static_cast<int>(n_heads) : 16) : p.q_rows;
-    const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
+    const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(p.q_rows), 1};
     if ((s = encode_nd(q, bf16, 3, gdim, gst, box, &p.tm_q)) != SDPA_OK) return s;
   }
   p.out = out;

@@ -56,7 +56,7 @@ struct MaskTilesParams {
 // Sparse top-k attention: query row i (all heads of head group g) attends to
 // the key rows idx[i, 0 .. len_i) of one shared key/value head.
 struct SparseParams {
-  CUtensorMap tm_q;  // 3-D (D, H, total_q), box 64 x min(H, 128) x 1 (one head group; see q_half)
+  CUtensorMap tm_q;  // 3-D (D, H, total_q), box 64 x min(H, 128) x 1 (one head group)
   void* out;                // [total_q, H, D]
   int64_t o_st, o_sh;
   float* lse;               // optional [total_q, H]
@@ -66,10 +66,9 @@ struct SparseParams {
   const int* topk_length;   // [total_q] valid leading entries, or null (all topk)
   int total_q, total_k, H, topk, n_groups;
   int q_rows;               // heads of a group: min(H, 128)
-  // 1 (H <= 64): head h of the group sits in tile row 32 (h / 16) + h % 16,
-  // loaded as boxes of min(16, H) rows (tm_q's box is 64 x min(16, H) x 1),
-  // and two threads share each row; 0: rows 0 .. q_rows - 1, one box of
-  // q_rows rows, one thread a row
+  // 1 (H <= 64): M = 64 products, which put head h in TMEM lane
+  // 32 (h / 16) + h % 16, and two softmax threads share each row; 0: M = 128
+  // products, one thread a row
   int q_half;
   int kv_shared;            // 1: k and v are one tensor (gather once, use twice)
   const void* k;            // [total_k, D] rows for the gathers

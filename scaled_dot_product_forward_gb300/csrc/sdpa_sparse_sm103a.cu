@@ -301,9 +301,10 @@ __device__ __forceinline__ void finish_row(const sdpa_impl::SparseParams& p, uin
   store_row<D, BF16>(t_o, inv_l, orow, h < p.H);
 }
 
-// ---- The half-row form (groups of at most 64 heads).  Head h of the group
-// sits in TMEM lane 32 (h / 16) + h % 16, so each warp of the softmax
-// warpgroup owns 16 rows, and threads t and t + 16 share row t: keys
+// ---- The half-row form (groups of at most 64 heads).  The products are
+// M = 64 tcgen05.mma, which put row h of the group in TMEM lane
+// 32 (h / 16) + h % 16, so each warp of the softmax warpgroup owns 16 rows
+// (its quarter's first half), and threads t and t + 16 share row t: keys
 // [0, 64) and [64, 128) of every tile, and the first and second halves of
 // the row's accumulator columns.
 
@@ -465,9 +466,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     bars->abort_flag = 0;
     fence_barrier_init();
   }
-  if (HALF) {
-    // rows of the Q tile that hold no head are never loaded: zero them once,
-    // so the products read finite values there
+  if (HALF && p.q_rows < 64) {
+    // rows H .. 63 of the Q tile (read by the M = 64 products) are never
+    // loaded: zero them once, so the products read finite values there
     for (int i = threadIdx.x; i < Lay::kTileBytes / 16; i += kThreads)
       reinterpret_cast<uint4*>(sQ)[i] = make_uint4(0, 0, 0, 0);
     fence_proxy_async_smem();
@@ -627,22 +628,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (job.n_kv == 0) continue;
       if (jobs > 0 && !warp_swait(&bars->q_empty, (jobs - 1) & 1, bars, limit, kSpEmpty)) break;
       if (leader) {
-        if (HALF) {
-          // heads 16 i .. 16 i + 15 into rows 32 i .. 32 i + 15
-          const int box = min(16, p.H), n_box = (p.H + 15) / 16;
-          mbar_arrive_expect_tx(&bars->q_full, Lay::kChunks * n_box * box * 128);
+        mbar_arrive_expect_tx(&bars->q_full, Lay::kChunks * p.q_rows * 128);
 #pragma unroll
-          for (int c = 0; c < Lay::kChunks; ++c)
-            for (int i = 0; i < n_box; ++i)
-              tma_load_3d(sQ + c * Lay::kChunkBytes + i * 32 * 128, &p.tm_q, &bars->q_full,
-                          c * 64, i * 16, job.row);
-        } else {
-          mbar_arrive_expect_tx(&bars->q_full, Lay::kChunks * p.q_rows * 128);
-#pragma unroll
-          for (int c = 0; c < Lay::kChunks; ++c)
-            tma_load_3d(sQ + c * Lay::kChunkBytes, &p.tm_q, &bars->q_full, c * 64,
-                        job.group * kRows, job.row);
-        }
+        for (int c = 0; c < Lay::kChunks; ++c)
+          tma_load_3d(sQ + c * Lay::kChunkBytes, &p.tm_q, &bars->q_full, c * 64,
+                      job.group * kRows, job.row);
       }
       ++jobs;
     }
@@ -729,8 +719,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     cp_async_wait<0>();
   } else if (warp == 1) {
     // ------------------------------------------------------ MMA issue
-    constexpr uint32_t idS = idesc_f16_f32acc(BF16, false, kRows, kKeys);
-    constexpr uint32_t idPV = idesc_f16_f32acc(BF16, true, kRows, D);
+    // The half-row form issues M = 64 products: row r of the 64-row Q tile
+    // (and of P, O) lives in TMEM lane 32 (r / 16) + r % 16.
+    constexpr uint32_t idS = idesc_f16_f32acc(BF16, false, HALF ? 64 : kRows, kKeys);
+    constexpr uint32_t idPV = idesc_f16_f32acc(BF16, true, HALF ? 64 : kRows, D);
     constexpr uint32_t kHi = desc_hi_sw128(1024);
     const uint32_t q_lo = desc_lo_sw128(smem_addr(sQ), 16);
     const uint32_t k_lo = desc_lo_sw128(smem_addr(sK), 16);

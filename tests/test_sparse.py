@@ -153,9 +153,9 @@ def test_one_kv_tensor_for_keys_and_values(sdpa_lib):
 
 HALF_ROW_CASES = [  # total_q, total_k, H, D, topk, dtype -- groups of at most 64 heads
     (1, 500, 64, 128, 300, torch.bfloat16),    # one row
-    (7, 800, 48, 128, 200, torch.float16),     # three 16-head boxes
-    (9, 700, 20, 128, 150, torch.bfloat16),    # the second box runs past the heads
-    (5, 300, 8, 64, 100, torch.float16),       # fewer heads than one box
+    (7, 800, 48, 128, 200, torch.float16),     # the last quarter of the tile holds no head
+    (9, 700, 20, 128, 150, torch.bfloat16),    # a quarter holds 4 of its 16 heads
+    (5, 300, 8, 64, 100, torch.float16),       # fewer heads than one quarter
     (29, 1200, 32, 64, 640, torch.bfloat16),   # head size 64, ragged last tiles
 ]
 
@@ -163,8 +163,8 @@ HALF_ROW_CASES = [  # total_q, total_k, H, D, topk, dtype -- groups of at most 6
 @pytest.mark.parametrize("case", HALF_ROW_CASES,
                          ids=[f"q{c[0]}-k{c[1]}-H{c[2]}-D{c[3]}-topk{c[4]}" for c in HALF_ROW_CASES])
 def test_half_row_form_matches_oracle(sdpa_lib, case):
-    """Groups of at most 64 heads put 16 heads in each quarter of the tile and
-    split every row's keys between two softmax threads."""
+    """Groups of at most 64 heads run M = 64 products (16 heads in each
+    quarter of TMEM) and split every row's keys between two softmax threads."""
     total_q, total_k, H, D, topk, dtype = case
     q, k, v, idx, length = make(*case, seed=1400 + H + D + total_q)
     dev = torch.device("cuda")
