@@ -520,6 +520,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       float m_used = -INFINITY, l = 0.0f;
       for (int j = 0; j < job.n_kv; ++j) {
+        // The tile's key mask first: it is written when the tile is gathered,
+        // long before its S, so this read overlaps the wait for S.  The
+        // gathers refill this mask slot (mask slots = stages + 2) only once
+        // the stage of the tile two after this one is free again, which needs
+        // that tile's P and so this tile's: m_full of the slot is at most one
+        // phase ahead of this wait.
+        uint32_t km[4];
+        if (!warp_swait(&bars->m_full[mslot.idx], mslot.phase, bars, limit, kSpK)) {
+          ok = false;
+          break;
+        }
+        {
+          const volatile uint32_t* src = bars->kmask[mslot.idx];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) km[e] = src[e];
+        }
+        mslot.next(n_slots);
         const uint32_t b = ns & 1;
         if (!warp_swait(&bars->s_full[b], (ns >> 1) & 1, bars, limit, kSpS)) {
           ok = false;
@@ -542,21 +559,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c = 0; c < kPer; ++c) s[c] = __uint_as_float(su[c]);
         }
-        // The gathers refill this mask slot (mask slots = stages + 2) only
-        // once the stage of the tile two after this one is free again, which
-        // needs that tile's P and so this tile's: m_full of the slot is at
-        // most one phase ahead of this wait.
-        uint32_t km[4];
-        if (!warp_swait(&bars->m_full[mslot.idx], mslot.phase, bars, limit, kSpK)) {
-          ok = false;
-          break;
-        }
-        {
-          const volatile uint32_t* src = bars->kmask[mslot.idx];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) km[e] = src[e];
-        }
-        mslot.next(n_slots);
         bool need;
         uint32_t pk[kPer / 2];
         float alpha;
