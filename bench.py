@@ -44,8 +44,14 @@ if ROOT not in sys.path:
 METRIC = "causal SDPA fwd TFLOP/s at B4·H32·L4096·D128 bf16; % of GB300 tensor peak"
 UNIT = "TFLOP/s"
 FALLBACK_BF16_TFLOPS = 1900.0
+# The code each kernel is built from (a traffic figure is valid only for the
+# code it was captured on): head size 128, head size 64, sparse top-k.
 KERNEL_SOURCES = ["scaled_dot_product_forward_gb300/csrc/sdpa_fwd_sm103a.cu",
+                  "scaled_dot_product_forward_gb300/csrc/sdpa_sched.cuh",
                   "scaled_dot_product_forward_gb300/csrc/ptx.cuh"]
+KERNEL64_SOURCES = ["scaled_dot_product_forward_gb300/csrc/sdpa_fwd64_sm103a.cu",
+                    "scaled_dot_product_forward_gb300/csrc/sdpa_sched.cuh",
+                    "scaled_dot_product_forward_gb300/csrc/ptx.cuh"]
 SPARSE_SOURCES = ["scaled_dot_product_forward_gb300/csrc/sdpa_sparse_sm103a.cu",
                   "scaled_dot_product_forward_gb300/csrc/ptx.cuh"]
 
@@ -696,7 +702,8 @@ def dense_line(args, wid, rank, world):
     peak, hbm_peak, peak_kind = load_peaks()
     # A masked plan runs the mask-summary path (its own ncu capture).
     summary = (args.plan or args.graph) and w.p_masked is not None
-    traffic = load_traffic(f"{wid}plan" if summary else wid)
+    traffic = load_traffic(f"{wid}plan" if summary else wid,
+                           KERNEL64_SOURCES if w.D == 64 else KERNEL_SOURCES)
     e2e_ms = max_over_ranks(r["e2e_ms"], world)
     line = {"metric": metric_of(w), "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
