@@ -11,20 +11,23 @@
 //
 // Forward, built the way the dense kernel is, for one shared key set per query
 // row instead of one per tile:
-//   * a job is one query row and a group of up to 128 of its heads: the heads
-//     are the 128 rows of the tensor-core tile (M = 128; groups of fewer heads
-//     are zero-padded by the tensor map), and they share the gathered keys;
-//   * warp 0 loads the job's Q with a 3-D TMA box; warps 2 and 3 gather the
-//     K and V rows by index with coalesced 16-byte cp.async copies (128 keys
-//     per stage, a whole row per instruction group) into the swizzled layout
-//     the tensor core reads, after checking every index (entries past the
-//     row's count or out of range become row 0 and are removed in the
-//     softmax); with one kv tensor the rows are gathered once;
+//   * a job is one query row and a group of up to 128 of its heads, which
+//     share the gathered keys; groups of more than 64 heads are the 128 rows
+//     of M = 128 products, one softmax thread a row; groups of at most 64
+//     take M = 64 products (head h in TMEM lane 32 (h / 16) + h % 16) and two
+//     softmax threads a row, so no thread works on rows the group lacks;
+//   * warp 0 loads the job's Q with a 3-D TMA box; warps 8..11 gather the K
+//     and V rows by index with coalesced 16-byte cp.async copies (128 keys per
+//     stage) into the swizzled layout the tensor core reads, after checking
+//     every index (entries past the row's count or out of range become row 0
+//     and are removed in the softmax), and announce each stage through the
+//     copy unit when its rows have landed; with one kv tensor the rows are
+//     gathered once;
 //   * warp 1 issues S = Q K^T into two alternating TMEM buffers, so S(j+1)
 //     runs while the softmax works on S(j), and O += P V with P in its own
-//     TMEM columns;
-//   * warpgroup 1 runs the online softmax, one head row per thread, as in the
-//     dense kernel, and writes O / l and the log-sum-exp.
+//     double-buffered TMEM columns;
+//   * warpgroup 1 runs the online softmax and writes O / l and the
+//     log-sum-exp.
 // Every barrier wait is bounded in time; on expiry the CTA records a status
 // bit (read with the dense kernel's by sdpa_last_device_status), stops and
 // frees its tensor memory.
@@ -43,7 +46,7 @@ namespace {
 constexpr int kRows = 128;     // head rows per job (TMEM lanes)
 constexpr int kKeys = 128;     // gathered keys per stage
 constexpr int kThreads = 384;  // WG0: Q loads, MMA, 2 idle; WG1: softmax; WG2: gathers
-constexpr int kGatherWarps = 4;  // warps 8..11: one key row per thread
+constexpr int kGatherWarps = 4;  // warps 8..11: 32 key rows each
 // Register split: the launch reserves kLaunchRegs per thread (the cap of
 // __launch_bounds__(384, 1)); the softmax warpgroup takes registers from the
 // other two.  128*232 + 256*136 == 384*168.
@@ -89,9 +92,9 @@ struct SBarriers {
   // (a stage's K and V rows are copied as one group and announced together
   // by k_full)
   uint64_t v_empty[kMaxStages];
-  // Validity of the 128 gathered keys of K tile g, in slot g % kMaskSlots:
-  // word w bit i = key 32w + i; m_full[slot] completes when both gather
-  // warps have written their words.
+  // Validity of the 128 gathered keys of a tile, in the next slot of a ring
+  // of stages + 2: word w bit i = key 32w + i; m_full[slot] completes when
+  // all four gather warps have written their words.
   uint64_t m_full[kMaxStages + 2];
   uint32_t kmask[kMaxStages + 2][4];
   uint32_t tmem_base;
@@ -583,15 +586,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           else
             rescale_row<D>(tmem + kColO + lane_off, alpha);
         }
-        // P buffer t & 1 is free once PV(t-2) is done.
+        // P buffer t & 1 is free once PV(t-2) is done, which S(t) being
+        // complete implies: the issuing warp issued S(t) after PV(t-2), and a
+        // commit completes only after every earlier product.  (The o_done
+        // waits that remain cannot fall two phases behind: a barrier's next
+        // phase needs this tile's P.)
         const uint32_t pb = t & 1;
-        if (t >= 2) {
-          if (!warp_swait(&bars->o_done[pb], ((t >> 1) - 1) & 1, bars, limit, kSpO)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-        }
         if constexpr (HALF) {
           tmem_st16x2_32<kKeys / 4>(tmem + kColP + pb * 64 + lane_off, pk);
         } else {
