@@ -207,3 +207,29 @@ def test_negative_scale(sdpa_lib):
     assert sdpa_lib.sdpa_last_device_status()[0] == 0
     check(out.double().cpu().numpy(),
           oracle.sdpa_sparse(q, k, v, idx, topk_length=length, scale=-0.2), "negative scale")
+
+
+ONE_KV_CASES = [  # total_q, total_k, H, D, topk, dtype -- one tensor as keys and values
+    (21, 1400, 128, 128, 520, torch.bfloat16),  # more than 64 heads: M = 128 products
+    (17, 900, 48, 64, 300, torch.float16),      # head size 64, half-row form
+]
+
+
+@pytest.mark.parametrize("case", ONE_KV_CASES,
+                         ids=[f"q{c[0]}-k{c[1]}-H{c[2]}-D{c[3]}-topk{c[4]}" for c in ONE_KV_CASES])
+def test_one_kv_tensor_matches_oracle(sdpa_lib, case):
+    """One kv tensor (rows gathered once into a deeper ring) on the paths
+    the benchmark workload does not take."""
+    total_q, total_k, H, D, topk, dtype = case
+    q, kv, _, idx, length = make(*case, seed=1440 + H + D)
+    dev = torch.device("cuda")
+    kvd = kv.to(dev)
+    out, lse = sdpa_lib.sdpa_sparse_forward(q.to(dev), kvd, kvd, torch.from_numpy(idx).to(dev),
+                                            torch.from_numpy(length).to(dev), return_lse=True)
+    assert sdpa_lib.sdpa_last_device_status()[0] == 0
+    ref, ref_lse = oracle.sdpa_sparse(q, kv, kv, idx, topk_length=length, return_lse=True)
+    check(out.double().cpu().numpy(), ref, "one kv tensor")
+    got_lse = lse.double().cpu().numpy()
+    fin = np.isfinite(ref_lse)
+    assert np.array_equal(np.isfinite(got_lse), fin)
+    np.testing.assert_allclose(got_lse[fin], ref_lse[fin], rtol=0, atol=2e-3)
