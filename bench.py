@@ -91,7 +91,8 @@ def roofline_of(w, flops, mean_launch_ms, peak, hbm_peak, peak_kind, traffic):
     measured peaks: the tensor core (TFLOP/s against the bf16 GEMM rate) when
     its algorithmic FLOP per algorithmic byte is at or above the ridge, else
     HBM (GB/s of algorithmic bytes against the measured copy bandwidth)."""
-    alg_bytes = w.alg_bytes()
+    # (a rank with a range of the heads moves that share of the bytes)
+    alg_bytes = w.alg_bytes() * flops / w.flops()
     tflops = flops / (mean_launch_ms * 1e-3) / 1e12
     gbs = alg_bytes / (mean_launch_ms * 1e-3) / 1e9
     ridge = peak * 1e12 / (hbm_peak * 1e9) if hbm_peak > 0 else 0.0
@@ -332,11 +333,20 @@ def gpu_leg(args, w, rank, world):
     torch.cuda.set_device(dev)
     sdpa.load_library()
     q, k, v, mask = sdpa_inputs.make(w)
+    flops = w.flops()
+    if getattr(args, "shard", "replicas") == "heads" and world > 1:
+        # This rank's contiguous range of the heads of the one problem (the
+        # heads are independent: no exchange), held as its own tensors.
+        if world > w.H:
+            raise SystemExit(f"--shard heads: {world} ranks for {w.H} heads")
+        h0, h1 = sdpa.head_range(w.H, rank, world)
+        hd = 1 if q.dim() == 4 else 0
+        q, k, v = (x.narrow(hd, h0, h1 - h0).contiguous() for x in (q, k, v))
+        flops = w.flops() * (h1 - h0) / w.H
     qd, kd, vd = (x.to(dev) for x in (q, k, v))
     md = mask.to(dev) if mask is not None else None
     out = torch.empty_like(qd)
     stream = torch.cuda.Stream(dev)
-    flops = w.flops()
 
     def step():
         sdpa.sdpa_forward(qd, kd, vd, out, is_causal=w.is_causal, mask=md, stream=stream)
@@ -587,6 +597,9 @@ def max_over_ranks(x: float, world: int) -> float:
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--shard", choices=["replicas", "heads"], default="replicas",
+                    help="with N > 1: every rank runs the whole workload (weak scaling), or "
+                         "each computes its range of the heads of one problem (strong)")
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--workload", type=int, default=3)
@@ -697,7 +710,11 @@ def dense_line(args, wid, rank, world):
     r = gpu_leg(args, w, rank, world)
     total_ms = max_over_ranks(r["total_ms"], world)
     ms_per_step = total_ms / args.steps
-    value = world * r["flops"] / (ms_per_step * 1e-3) / 1e12
+    # replicas: every rank did the whole workload; heads: the ranks together
+    # did one (work of all ranks / the slowest rank's time either way)
+    sharded = args.shard == "heads" and world > 1
+    job_flops = w.flops() if sharded else world * r["flops"]
+    value = job_flops / (ms_per_step * 1e-3) / 1e12
     mean_launch_ms = statistics.fmean(r["per_launch_ms"])
     peak, hbm_peak, peak_kind = load_peaks()
     # A masked plan runs the mask-summary path (its own ncu capture).
@@ -707,11 +724,13 @@ def dense_line(args, wid, rank, world):
     e2e_ms = max_over_ranks(r["e2e_ms"], world)
     line = {"metric": metric_of(w), "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": dtype,
-            "data": "synthetic", "config": config_of(args, w),
+            "higher_is_better": True, "scaling": "strong" if sharded else "weak",
+            "vs_baseline": None, "dtype": dtype,
+            "data": "synthetic", "config": dict(config_of(args, w), parallelism=(
+                f"heads split over {world} ranks" if sharded else f"{world} replicas")),
             "roofline": roofline_of(w, r["flops"], mean_launch_ms, peak, hbm_peak, peak_kind,
-                                    traffic),
-            "e2e": {"value": world * r["flops"] / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+                                    traffic * r["flops"] / w.flops() if traffic else traffic),
+            "e2e": {"value": job_flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
                     "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"],
                     "ms_per_step": e2e_ms},
             "gpu_launches": args.steps * (2 if (args.graph or args.plan) and

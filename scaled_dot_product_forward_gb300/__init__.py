@@ -21,7 +21,8 @@ __all__ = ["sdpa_forward", "sdpa_forward_raw", "sdpa_status_string", "sdpa_last_
            "sdpa_version", "SdpaError", "load_library", "LIB_PATH", "STATUS",
            "sdpa_debug_set_wait_limit_ns", "sdpa_debug_withhold_q_load",
            "sdpa_forward_varlen", "sdpa_sparse_forward", "sdpa_sparse_compact", "SdpaPlan",
-           "sdpa_mask_tiles", "sdpa_forward_masked_noalloc"]
+           "sdpa_mask_tiles", "sdpa_forward_masked_noalloc", "head_range",
+           "sdpa_forward_heads"]
 
 LIB_PATH = _build.LIB_PATH
 
@@ -462,6 +463,32 @@ def sdpa_last_device_status(stream=None):
     rc = load_library().sdpa_last_device_status_detail(ctypes.c_void_p(st) if st else None,
                                                        ctypes.byref(detail))
     return int(rc), int(detail.value)
+
+
+def head_range(n_heads: int, rank: int, world: int) -> tuple[int, int]:
+    """Heads ``[h0, h1)`` of rank ``rank`` among ``world`` ranks: contiguous
+    ranges, the first ``n_heads % world`` ranks one head more.  Every (batch,
+    head) of the forward is independent, so ranks that each compute their
+    range of the same problem produce the whole output between them with no
+    exchange (a rank may get no head when world > n_heads)."""
+    if world < 1 or not 0 <= rank < world or n_heads < 0:
+        raise ValueError(f"rank {rank} of {world} ranks, {n_heads} heads")
+    base, extra = divmod(n_heads, world)
+    h0 = rank * base + min(rank, extra)
+    return h0, h0 + base + (1 if rank < extra else 0)
+
+
+def sdpa_forward_heads(q, k, v, out, h0: int, h1: int, **kw):
+    """``sdpa_forward`` on heads ``[h0, h1)`` only: q, k, v and out
+    ([B, H, L, D] or [H, L, D]) are narrowed to those heads as strided views,
+    so the call reads and writes that range in place.  Returns ``out``."""
+    hd = 1 if q.dim() == 4 else 0
+    if not 0 <= h0 <= h1 <= q.shape[hd]:
+        raise SdpaError(3)
+    if h0 < h1:
+        sdpa_forward(q.narrow(hd, h0, h1 - h0), k.narrow(hd, h0, h1 - h0),
+                     v.narrow(hd, h0, h1 - h0), out.narrow(hd, h0, h1 - h0), **kw)
+    return out
 
 
 def default_scale(D: int) -> float:
