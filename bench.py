@@ -551,33 +551,52 @@ def extra_leg(args, path):
                     "ms_per_step": e2e_ms},
             "gpu_launches": args.steps, "clocks": clk, "parity": None}
     if not args.no_cpu_baseline:
-        # the oracle on a bounded sample: one document / a few query rows
         # the oracle on a bounded sample, whose outputs also check the same
         # rows of the timed launches' output
+        import numpy as np
         import oracle
-        t0 = time.perf_counter()
+        # random (document, head) pairs / random query rows until the oracle
+        # has run for the budget (only the oracle calls are timed)
+        gen = torch.Generator().manual_seed(4242)
+        refs, gots = [], []
+        f, t, rows, units = 0.0, 0.0, 0, 0
+        out_h = out.cpu()
         if path == "varlen":
-            d = min(range(len(lengths)), key=lambda i: lengths[i])
-            a, n = int(cu[d]), lengths[d]
-            ref = oracle.sdpa_varlen(q[a:a + n, :1], k[a:a + n, :1], v[a:a + n, :1], [0, n],
-                                     is_causal=True)
-            got = out[a:a + n, :1]
-            f = 2.0 * 1 * n * n * D
-            sample = f"head 0 of the shortest document ({n} tokens)"
-            rows = n
+            for pid in torch.randperm(len(lengths) * H, generator=gen).tolist():
+                d, hh = divmod(pid, H)
+                a, n = int(cu[d]), lengths[d]
+                t0 = time.perf_counter()
+                ref = oracle.sdpa_varlen(q[a:a + n, hh:hh + 1], k[a:a + n, hh:hh + 1],
+                                         v[a:a + n, hh:hh + 1], [0, n], is_causal=True)
+                t += time.perf_counter() - t0
+                refs.append(np.asarray(ref).reshape(-1, D))
+                gots.append(out_h[a:a + n, hh:hh + 1].double().numpy().reshape(-1, D))
+                f += 2.0 * n * n * D
+                rows += n
+                units += 1
+                if t >= args.cpu_budget_s:
+                    break
+            sample = f"{units} random (document, head) pairs, {rows} rows"
         else:
-            rows = 64
-            sel = torch.arange(q.shape[0] - rows, q.shape[0])
-            ref = oracle.sdpa_sparse(q[sel], kv, kv, idx[sel].numpy(),
-                                     topk_length=length[sel].numpy())
-            got = out[sel.to(dev)]
-            f = 4.0 * H * D * float(length[sel].sum())
-            sample = f"the last {rows} query rows (all heads)"
-        t = time.perf_counter() - t0
+            perm = torch.randperm(q.shape[0], generator=gen)
+            for c0 in range(0, q.shape[0], 128):
+                sel = perm[c0:c0 + 128]
+                t0 = time.perf_counter()
+                ref = oracle.sdpa_sparse(q[sel], kv, kv, idx[sel].numpy(),
+                                         topk_length=length[sel].numpy())
+                t += time.perf_counter() - t0
+                refs.append(np.asarray(ref).reshape(-1, D))
+                gots.append(out_h[sel].double().numpy().reshape(-1, D))
+                f += 4.0 * H * D * float(length[sel].sum())
+                rows += len(sel)
+                if t >= args.cpu_budget_s:
+                    break
+            sample = f"{rows} random query rows (all heads)"
+        ref, got = np.concatenate(refs), np.concatenate(gots)
         line["cpu_baseline"] = {"value": f / t / 1e12, "unit": UNIT,
                                 "cores": oracle.num_threads(), "kind": "oracle",
                                 "sample": f"{sample}, {t:.1f} s"}
-        line["parity"] = parity_of(got.double().cpu().numpy(), ref, rows,
+        line["parity"] = parity_of(got, ref, rows,
                                    "fp64 oracle on the cpu_baseline sample of the timed "
                                    "launches' output")
     return line
