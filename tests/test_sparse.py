@@ -157,6 +157,7 @@ HALF_ROW_CASES = [  # total_q, total_k, H, D, topk, dtype -- groups of at most 6
     (9, 700, 20, 128, 150, torch.bfloat16),    # a quarter holds 4 of its 16 heads
     (5, 300, 8, 64, 100, torch.float16),       # fewer heads than one quarter
     (29, 1200, 32, 64, 640, torch.bfloat16),   # head size 64, ragged last tiles
+    (6, 5000, 64, 128, 4100, torch.bfloat16),  # 33 key tiles a row: many laps of the ring
 ]
 
 
