@@ -602,6 +602,13 @@ def extra_leg(args, path):
     return line
 
 
+def job_flops(workload_flops: float, rank_flops: float, world: int, sharded: bool) -> float:
+    """The work one timed step of the whole job did: with replicas every rank
+    ran the workload (rank_flops each); with the heads split the ranks
+    together ran it once."""
+    return workload_flops if (sharded and world > 1) else world * rank_flops
+
+
 def max_over_ranks(x: float, world: int) -> float:
     if world <= 1:
         return x
@@ -732,8 +739,8 @@ def dense_line(args, wid, rank, world):
     # replicas: every rank did the whole workload; heads: the ranks together
     # did one (work of all ranks / the slowest rank's time either way)
     sharded = args.shard == "heads" and world > 1
-    job_flops = w.flops() if sharded else world * r["flops"]
-    value = job_flops / (ms_per_step * 1e-3) / 1e12
+    done = job_flops(w.flops(), r["flops"], world, sharded)
+    value = done / (ms_per_step * 1e-3) / 1e12
     mean_launch_ms = statistics.fmean(r["per_launch_ms"])
     peak, hbm_peak, peak_kind = load_peaks()
     # A masked plan runs the mask-summary path (its own ncu capture).
@@ -749,7 +756,7 @@ def dense_line(args, wid, rank, world):
                 f"heads split over {world} ranks" if sharded else f"{world} replicas")),
             "roofline": roofline_of(w, r["flops"], mean_launch_ms, peak, hbm_peak, peak_kind,
                                     traffic * r["flops"] / w.flops() if traffic else traffic),
-            "e2e": {"value": job_flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+            "e2e": {"value": done / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
                     "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"],
                     "ms_per_step": e2e_ms},
             "gpu_launches": args.steps * (2 if (args.graph or args.plan) and

@@ -98,3 +98,16 @@ def test_head_ranges_reproduce_the_whole_call(sdpa_lib, world):
     torch.cuda.synchronize()
     assert sdpa_lib.sdpa_last_device_status()[0] == 0
     assert torch.equal(out, whole)
+
+
+def test_job_rate_counts_the_work_once_when_sharded():
+    import bench
+    from scaled_dot_product_forward_gb300 import head_range
+    total = 5.5e11
+    # heads split over 3 ranks: each did its share, the job did the workload once
+    shares = [total * (h1 - h0) / 32 for h0, h1 in (head_range(32, r, 3) for r in range(3))]
+    assert abs(sum(shares) - total) < 1.0
+    assert bench.job_flops(total, shares[0], 3, sharded=True) == total
+    # replicas: every rank ran the whole workload
+    assert bench.job_flops(total, total, 4, sharded=False) == 4 * total
+    assert bench.job_flops(total, total, 1, sharded=True) == total

@@ -40,6 +40,7 @@ def make(total_q, total_k, H, D, topk, dtype, seed, empty_rows=True):
 
 CASES = [  # total_q, total_k, H, D, topk, dtype
     (40, 3000, 128, 128, 300, torch.bfloat16),
+    (15, 700, 160, 128, 300, torch.bfloat16),   # two head groups: 128 and 32
     (33, 2000, 64, 128, 1000, torch.bfloat16),
     (50, 1500, 16, 64, 257, torch.float16),
     (20, 900, 192, 64, 128, torch.bfloat16),
