@@ -363,8 +363,9 @@ SDPA_API int sdpa_version(void);
  * Test hooks (not for production use).
  * sdpa_debug_set_wait_limit_ns: bound on a single barrier wait inside the
  *   kernel (default 1e9 ns); 0 restores the default.
- * sdpa_debug_withhold_q_load: when nonzero, subsequent launches never load
- *   the query tile, so every consumer wait runs out: the kernel must return
+ * sdpa_debug_withhold_q_load: when nonzero, subsequent launches (dense,
+ *   packed-document and sparse forwards) never load the query tile, so every
+ *   consumer wait runs out before any product is issued: the kernel must return
  *   with SDPA_ERR_DEVICE_TIMEOUT reported by sdpa_last_device_status and the
  *   context must stay usable.
  */

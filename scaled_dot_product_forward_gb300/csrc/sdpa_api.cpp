@@ -614,6 +614,7 @@ sdpa_status sdpa_sparse_forward(const void* q, const void* k, const void* v, voi
                                       : static_cast<double>(scale);
   p.scale_log2 = static_cast<float>(sc * 1.4426950408889634);
   if (p.scale_log2 == 0.0f) p.scale_log2 = std::signbit(sc) ? -FLT_MIN : FLT_MIN;
+  p.debug_withhold_q = g_withhold_q.load(std::memory_order_relaxed);
   p.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
   const int sms = g_device_sms[dev].load(std::memory_order_relaxed);
   const cudaError_t e = sdpa_impl::launch_sparse(p, static_cast<int>(head_dim), bf16, sms,

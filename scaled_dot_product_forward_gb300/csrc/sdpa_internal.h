@@ -75,6 +75,7 @@ struct SparseParams {
   const void* v;
   int64_t k_row_bytes, v_row_bytes;
   float scale_log2;
+  int debug_withhold_q;     // test hook: 1 = never load Q, so every consumer wait runs out
   uint64_t wait_limit_ns;
 };
 

@@ -629,7 +629,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int jj = static_cast<int>(blockIdx.x); job_of(p, jj, job); jj += step) {
       if (job.n_kv == 0) continue;
       if (jobs > 0 && !warp_swait(&bars->q_empty, (jobs - 1) & 1, bars, limit, kSpEmpty)) break;
-      if (leader) {
+      if (leader && !p.debug_withhold_q) {
         mbar_arrive_expect_tx(&bars->q_full, Lay::kChunks * p.q_rows * 128);
 #pragma unroll
         for (int c = 0; c < Lay::kChunks; ++c)
@@ -638,7 +638,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       ++jobs;
     }
-    if (jobs > 0) swait(&bars->q_full, (jobs - 1) & 1, bars, limit, kSpDrain, false);
+    if (jobs > 0 && !p.debug_withhold_q)
+      swait(&bars->q_full, (jobs - 1) & 1, bars, limit, kSpDrain, false);
   } else if (warp >= 8) {
     // ------------------------------------------------- key/value gathers
     // Warp w (8..11) copies key rows 32(w-8) .. +31 of every tile, 16 bytes
